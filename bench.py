@@ -1,0 +1,489 @@
+"""Benchmark of the fused reduce + residual + RMSNorm step on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...      # the CPU oracle, timed on host cores
+    python bench.py --sweep                   # SM-budget x token-count table (many lines)
+
+A step is one pass of the hot path over one batch: the wave-aware split plan
+(tw_wave_split, host) and the fused step over the batch (tw_run_split: prefix
+on one stream, suffix on another; at T=1024 the plan keeps the batch whole).
+The default workload is the Llama-3.3-70B layer shape, T=1024 tokens, H=8192,
+N=8 partial buffers. Inputs rotate among enough seeded sets to exceed 4x the
+L2 cache, so no step reads inputs the previous step left in L2.
+
+Rank 0 prints ONE JSON line. ``value`` is whole-job algorithmic GB/s:
+(N+3)*T*H*2 + H*2 bytes per step, times the steps of all ranks, over the
+slowest rank's device time. With torchrun (N>1) every rank runs its own
+replica of the workload (the step has no cross-GPU exchange on one node's
+replicas), and the timing is the max over ranks.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused reduce+RMSNorm GB/s and % of GB300 HBM peak; tokens/s at T=1K–16K"
+PLANNER_SMS = 148  # SMs the planner models for the compute kernels (split workload)
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "reduce_rmsnorm_gb300", "csrc", "fused_kernel.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_kernel_traffic.json")
+
+
+# ------------------------------------------------------------------ small helpers
+
+
+def peak_hbm():
+    """(GB/s, source) of the HBM roofline denominator."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is for another kernel revision or workload."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_sha") != kernel_sha():
+        return None
+    w = d.get("workloads", {}).get(workload)
+    return None if w is None else int(w["dram_bytes_per_launch"])
+
+
+def ctas_unsplit(T, H):
+    """CTA count of the row-parallel projection the split plan models:
+    128-token x 128-column tiles, 8 ranks: ceil(T/128) * (H/128) / 8."""
+    return math.ceil(T / 128) * (H // 128) // 8
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index, period_ms=50):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc.stdout.readline()  # first sample: sampler is running
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), max=float(f[2]), power=float(f[3]),
+                                 hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+
+def dist_setup():
+    """(rank, world). Initialises torch.distributed when launched by torchrun."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    """Max of a float over ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, elapsed_s_max, world):
+    """Whole-job rate: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / elapsed_s_max
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+
+def make_sets(name, T_override, l2_bytes, device):
+    import torch
+    import synth
+    w = dict(synth.WORKLOADS[name])
+    if T_override:
+        w["T"] = T_override
+    T, H, N = w["T"], w["H"], w["N"]
+    per_set = (N + 2) * T * H * 2 + H * 2  # resident bytes of one set (inputs + output)
+    nsets = max(1, math.ceil(4 * l2_bytes / per_set))
+    sets = []
+    for k in range(nsets):
+        p, r, g = synth.make_inputs(seed=k, **w)
+        P = p.to(device)
+        sets.append(dict(P=P, plist=[P[i] for i in range(N)], R=r.to(device), G=g.to(device),
+                         out=torch.empty((T, H), dtype=torch.bfloat16, device=device)))
+    torch.cuda.synchronize()
+    return T, H, N, sets, per_set
+
+
+def gpu_arm(args, rank, world):
+    import torch
+    import reduce_rmsnorm_gb300 as tw
+    from reduce_rmsnorm_gb300 import build
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    build.build()
+    tw.lib()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    T, H, N, sets, per_set = make_sets(args.workload, args.tokens, l2, dev)
+    eps = 1e-5
+    C = ctas_unsplit(T, H)
+    bytes_step = tw.bytes_per_call(T, H, N)
+    sa = torch.cuda.current_stream(dev)
+    sb = torch.cuda.Stream(dev)
+
+    def step(k):
+        s = sets[k % len(sets)]
+        prefix, _ = tw.tw_wave_split(T, C, PLANNER_SMS)
+        tw.tw_run_split(prefix, s["plist"], s["R"], s["G"], eps, s["out"], sa, sb, args.sm_budget)
+        return prefix
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    prefix, suffix = tw.tw_wave_split(T, C, PLANNER_SMS)
+    launches_per_step = (1 if prefix > 0 else 0) + (1 if suffix > 0 else 0)
+
+    # per-step device durations on the launching stream (the step's kernels)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(sa)
+    for k in range(args.steps):
+        evs[k][0].record(sa)
+        step(args.warmup + k)
+        evs[k][1].record(sa)
+    t_end.record(sa)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    elapsed_ms_max = max_over_ranks(elapsed_ms, world)
+    value_gbs = job_throughput(bytes_step * args.steps, elapsed_ms_max / 1e3, world) / 1e9
+    assert tw.tw_device_status(reset=True) == 0, "a kernel gave up on a bounded wait"
+
+    peak, peak_src = peak_hbm()
+    mean_step_ms = statistics.fmean(step_ms)
+    achieved = bytes_step / (mean_step_ms / 1e3) / 1e9
+    traffic = ncu_traffic(args.workload if not args.tokens else None)
+
+    result = None
+    if rank == 0:
+        e2e = e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb)
+        cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(args.workload, args.tokens)
+        result = {
+            "metric": METRIC, "value": round(value_gbs, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_ms_max / args.steps, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+            "data": "synthetic (seeded N(0,sigma^2) partials, N(0,1) residual, N(1,0.1^2) gamma)",
+            "config": {"workload": args.workload, "T": T, "H": H, "N": N, "eps": eps,
+                       "sm_budget": args.sm_budget, "plan": [prefix, suffix],
+                       "planner": {"ctas_unsplit": C, "num_sms": PLANNER_SMS},
+                       "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "rotating %d input sets, %.1f MB total (L2 %.1f MB): inputs larger "
+                             "than 4x L2" % (len(sets), len(sets) * per_set / 1e6, l2 / 1e6)},
+            "tokens_per_s": round(T * args.steps * world / (elapsed_ms_max / 1e3), 1),
+            "hbm_frac": round(value_gbs / peak, 4),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_source": peak_src, "per": "launch (one fused call per step)"
+                         if launches_per_step == 1 else "step (%d concurrent launches)"
+                         % launches_per_step,
+                         "algorithmic_bytes": bytes_step,
+                         "step_us_median": round(statistics.median(step_ms) * 1e3, 3)},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+    return result
+
+
+def e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb):
+    """End to end through the public API with host buffers: every step copies
+    the step's inputs from pinned host memory, runs the plan and the fused
+    step, and copies the updated residual and the output back."""
+    import torch
+    import synth
+    w = dict(synth.WORKLOADS[args.workload])
+    if args.tokens:
+        w["T"] = args.tokens
+    p, r, g = synth.make_inputs(seed=100, **w)
+    hp, hr, hg = p.pin_memory(), r.pin_memory(), g.pin_memory()
+    hr_out = torch.empty_like(hr).pin_memory()
+    hy_out = torch.empty_like(hr).pin_memory()
+    P = torch.empty_like(p, device=dev)
+    R = torch.empty_like(r, device=dev)
+    G = torch.empty_like(g, device=dev)
+    out = torch.empty_like(R)
+    plist = [P[i] for i in range(N)]
+    steps = max(3, min(args.e2e_steps, args.steps))
+
+    def step():
+        P.copy_(hp, non_blocking=True)
+        R.copy_(hr, non_blocking=True)
+        G.copy_(hg, non_blocking=True)
+        prefix, _ = tw.tw_wave_split(T, C, PLANNER_SMS)
+        tw.tw_run_split(prefix, plist, R, G, eps, out, sa, sb, args.sm_budget)
+        hr_out.copy_(R, non_blocking=True)
+        hy_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(sa)
+    for _ in range(steps):
+        step()
+    b.record(sa)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = (N + 1) * T * H * 2 + H * 2
+    d2h = 2 * T * H * 2
+    return {"value": round(tw.bytes_per_call(T, H, N) / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(ms, 4)}
+
+
+# ------------------------------------------------------------------ the CPU oracle
+
+
+def _oracle_rows_timer(workload, T_override):
+    """Returns (T, H, N, time_rows(n) -> seconds) over the workload's first rows."""
+    import synth
+    from oracle import fused
+    w = dict(synth.WORKLOADS[workload])
+    if T_override:
+        w["T"] = T_override
+    T, H, N = w["T"], w["H"], w["N"]
+
+    def time_rows(n_rows, seed=0):
+        ww = dict(w)
+        ww["T"] = n_rows
+        p, r, g = synth.make_inputs(seed=seed, **ww)
+        pb, rb, gb = synth.bits(p), synth.bits(r), synth.bits(g)
+        t0 = time.perf_counter()
+        fused.reduce_residual_rmsnorm(pb, rb, gb, 1e-5)
+        fused.residual_fp32_rank_order(pb, rb)
+        return time.perf_counter() - t0
+
+    return T, H, N, time_rows
+
+
+def cpu_baseline(workload, T_override, budget_s=10.0):
+    """The oracle as it stands, on a bounded sample of the workload's rows."""
+    import reduce_rmsnorm_gb300 as tw
+    T, H, N, time_rows = _oracle_rows_timer(workload, T_override)
+    t1 = time_rows(8) / 8
+    rows = int(max(1, min(T, budget_s / max(t1, 1e-6) / 1.2)))
+    secs = time_rows(rows)
+    gbs = tw.bytes_per_call(rows, H, N) / secs / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "first %d of %d token rows of %s (fp64 NumPy oracle, one process), %.1f s"
+                      % (rows, T, workload, secs)}
+
+
+def reference_arm(args, rank, world):
+    """The oracle timed on the host cores as the reference arm: each step runs
+    the oracle on a bounded sample of the workload's rows."""
+    if rank != 0:
+        return None
+    import reduce_rmsnorm_gb300 as tw
+    T, H, N, time_rows = _oracle_rows_timer(args.workload, args.tokens)
+    t1 = time_rows(8) / 8
+    total_budget_s = 90.0
+    rows = int(max(1, min(T, total_budget_s / (args.steps + args.warmup) / max(t1, 1e-6))))
+    for k in range(args.warmup):
+        time_rows(rows, seed=k)
+    secs = [time_rows(rows, seed=args.warmup + k) for k in range(args.steps)]
+    total = sum(secs)
+    value = tw.bytes_per_call(rows, H, N) * args.steps / total / 1e9
+    sample = "first %d of %d token rows of %s per step (fp64 NumPy oracle, one process)" % (
+        rows, T, args.workload)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "T": T, "H": H, "N": N, "rows_per_step": rows},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+# ------------------------------------------------------------------ SM-budget sweep
+
+
+def sweep(args):
+    """GB/s and GB/s per SM for T = 512..16384 and budgets 2/4/8/16/full
+    (H=8192, N=8); one JSON line per cell."""
+    import torch
+    import reduce_rmsnorm_gb300 as tw
+    from reduce_rmsnorm_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak, _ = peak_hbm()
+    tokens = [int(t) for t in args.sweep_tokens.split(",")]
+    budgets = [int(b) for b in args.sweep_budgets.split(",")]
+    for T in tokens:
+        T_, H, N, sets, per_set = make_sets("llama70b_t1024_h8192_n8", T, l2, dev)
+        bytes_call = tw.bytes_per_call(T, H, N)
+        for budget in budgets:
+            reps = args.sweep_reps
+            for k in range(3):
+                s = sets[k % len(sets)]
+                tw.tw_fused_reduce_residual_rmsnorm(s["plist"], s["R"], s["G"], 1e-5, s["out"],
+                                                    sm_budget=budget)
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for k in range(reps):
+                s = sets[k % len(sets)]
+                evs[k][0].record()
+                tw.tw_fused_reduce_residual_rmsnorm(s["plist"], s["R"], s["G"], 1e-5, s["out"],
+                                                    sm_budget=budget)
+                evs[k][1].record()
+            torch.cuda.synchronize()
+            us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+            med = us[len(us) // 2]
+            used = tw.tw_launch_shape(T, H, N, budget)["grid"]
+            gbs = bytes_call / (med / 1e6) / 1e9
+            print(json.dumps({"T": T, "H": H, "N": N, "sm_budget": budget or "full",
+                              "sms_used": used, "us_median": round(med, 2),
+                              "us_p10": round(us[len(us) // 10], 2),
+                              "us_p90": round(us[(9 * len(us)) // 10], 2),
+                              "GB_s": round(gbs, 1), "GB_s_per_sm": round(gbs / used, 2),
+                              "hbm_frac": round(gbs / peak, 4),
+                              "tokens_per_s": round(T / (med / 1e6), 1), "sms": sms}),
+                  flush=True)
+        del sets
+        torch.cuda.empty_cache()
+    assert tw.tw_device_status(reset=True) == 0
+
+
+# ------------------------------------------------------------------ main
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="llama70b_t1024_h8192_n8")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's T")
+    ap.add_argument("--sm-budget", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-tokens", default="512,1024,2048,4096,8192,16384")
+    ap.add_argument("--sweep-budgets", default="2,4,8,16,0")
+    ap.add_argument("--sweep-reps", type=int, default=50)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.sweep:
+        sweep(args)
+        return
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; other ranks exit without work
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        res = reference_arm(args, rank, world)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    rank, world = dist_setup()
+    res = gpu_arm(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

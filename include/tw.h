@@ -1,0 +1,198 @@
+/*
+ * libtw -- fused reduce + residual + RMSNorm and wave-aware token splitting
+ * on one GPU (sm_103a).
+ *
+ * Pages cited (by title and section):
+ *   [W] "TokenWeave: Why Hiding Tensor-Parallel Communication Needs Wave
+ *       Arithmetic, Not Finer Tiles"
+ *   [G] "TokenWeave Guide: Compute-Communication Overlap for LLMs"
+ *
+ * Conventions shared by every call:
+ *   - Tensors are bf16, row-major and contiguous: a [T, H] tensor is T token
+ *     rows of H hidden values, row stride H elements. A shard or half of a
+ *     tensor is passed by offsetting its pointers by row0 * H elements.
+ *   - The caller owns every buffer. libtw allocates no device memory; it keeps
+ *     only per-device launch attributes (SM count, shared-memory limit).
+ *   - Launches are asynchronous on the stream(s) given; a device fault shows
+ *     at the caller's next synchronisation, as usual in CUDA. Work runs on the
+ *     device that is current on the calling thread.
+ *   - Arguments are validated before any CUDA call. Every call returns a
+ *     tw_status; no C++ exception crosses this boundary.
+ *   - A stream argument is a cudaStream_t; NULL is the legacy default stream.
+ */
+#ifndef TW_H
+#define TW_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* tw_stream_t; /* == cudaStream_t */
+
+/* Largest number of partial buffers (tensor-parallel ranks) one call sums. */
+#define TW_MAX_PARTIALS 16
+/* Largest hidden size: the kernel keeps a whole token row in registers. */
+#define TW_MAX_HIDDEN 32768
+
+typedef enum {
+  TW_OK = 0,
+  TW_ERR_INVALID_ARG = 1, /* null pointer, count or size out of range, overlap */
+  TW_ERR_ALIGN = 2,       /* H % 8 != 0 or a pointer not 16-byte aligned */
+  TW_ERR_UNSUPPORTED = 3, /* H > TW_MAX_HIDDEN */
+  TW_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  TW_ERR_DEVICE = 5       /* a kernel gave up on a bounded wait (see tw_device_status) */
+} tw_status;
+
+/*
+ * tw_fused_reduce_residual_rmsnorm -- the fused step.
+ *
+ * Defined by [W] "Fix two: RMSNorm was never insignificant" (the per-CTA
+ * sketch and its four numbered steps) and [G] "Fused AllReduce-RMSNorm:
+ * Bypassing Global Memory" / "The Standard RMSNorm Memory Round-Trip" (the
+ * RMSNorm formula). On one GPU the N tensor-parallel ranks' contributions are
+ * N buffers in this GPU's memory. For every token row t:
+ *
+ *     z       = ((P_0[t] + P_1[t]) + ... + P_{N-1}[t]) + R[t]   fp32, rank order
+ *     R[t]    = bf16_rne(z)                                       in place
+ *     r       = rsqrt( (sum_j z_j^2) / H + eps )                  fp32
+ *     out[t]  = bf16_rne( (z * r) * gamma )                       fp32, one rounding
+ *
+ * The sum of squares is taken on the unrounded fp32 z ([W] step 2). Rows are
+ * independent: any token-contiguous shard gives bitwise the same rows as the
+ * whole batch, and so does every sm_budget (the per-row arithmetic does not
+ * depend on the launch shape).
+ *
+ *   partials   host array of N device pointers, each bf16 [T, H], read only.
+ *              The array is read during the call only; partials may alias
+ *              one another.
+ *   N          1 .. TW_MAX_PARTIALS.
+ *   residual   device bf16 [T, H], read then overwritten with bf16(z).
+ *   gamma      device bf16 [H], read only.
+ *   eps        >= 0 and finite (1e-5 for the Llama workloads).
+ *   T          token rows, >= 0; T == 0 is a no-op returning TW_OK.
+ *   H          hidden size, 8 .. TW_MAX_HIDDEN, a multiple of 8.
+ *   out        device bf16 [T, H], written.
+ *   stream     the stream to launch on.
+ *   sm_budget  0: use the whole GPU (one CTA per SM). k > 0: launch at most k
+ *              CTAs, each owning one SM (it requests enough shared memory that
+ *              no second CTA of this kernel fits) and a contiguous range of
+ *              about T / k rows, so the step co-runs with work on the other
+ *              SMs ([W] "What it buys": 2 to 8 SMs). k above the SM count is
+ *              clamped. Negative is invalid.
+ *
+ * Errors: TW_ERR_INVALID_ARG (N, T, H <= 0, eps, sm_budget, a null pointer,
+ * residual/out overlapping each other or any input, T*H too large),
+ * TW_ERR_ALIGN (H % 8 or any pointer not 16-byte aligned), TW_ERR_UNSUPPORTED
+ * (H > TW_MAX_HIDDEN), TW_ERR_CUDA (device query or launch failure).
+ */
+int tw_fused_reduce_residual_rmsnorm(const void* const* partials, int N, void* residual,
+                                     const void* gamma, float eps, int64_t T, int64_t H,
+                                     void* out, tw_stream_t stream, int sm_budget);
+
+/*
+ * Offsets and threshold for tw_wave_split. Pass NULL for the pages' values:
+ * offsets {0, 64, 128, 192, 256, 512} and a 1024-token threshold ([W] "Fix
+ * one": the offline sweep's offsets and the dense-model threshold).
+ *   offsets          NULL (with n_offsets == 0): every integer 0 .. half-1.
+ *                    Otherwise n_offsets values >= 0 (both signs are tried).
+ *   min_split_tokens below this token count no split is made.
+ */
+typedef struct {
+  const int* offsets;
+  int n_offsets;
+  int min_split_tokens;
+} tw_split_opts;
+
+/*
+ * tw_wave_split -- wave-aware prefix/suffix split of a token batch.
+ *
+ * Defined by [W] "The overlap trap" (a kernel of c CTAs on S SMs runs in
+ * ceil(c / S) waves) and "Fix one: split at wave boundaries, unequally": the
+ * batch is split exactly twice, prefix = half + offset and suffix = half -
+ * offset with half = T / 2, and a split is admissible only if the waves of the
+ * two pieces do not exceed the waves of the unsplit kernel. The worked example
+ * (300 CTAs, 132 SMs: 132 / 168 in 3 waves, not 150 / 150 in 4) puts the
+ * smaller piece first, so each offset is tried with both signs.
+ *
+ * Reading of the rule (the pages give it in CTAs, the call works in tokens):
+ *   c(t)   = ceil(t * ctas_unsplit / num_tokens)   CTAs of a t-token piece
+ *   W      = ceil(ctas_unsplit / num_sms)          unsplit waves
+ *   admissible p: 0 < p < T and ceil(c(p)/S) + ceil(c(T-p)/S) <= W
+ *   choice: the smallest |offset|, ties to the smaller prefix.
+ *   no split, (T, 0), when T < min_split_tokens, W <= 1 (the single-wave
+ *   rule of "Fix one") or no candidate is admissible; (0, 0) for T == 0.
+ *
+ *   num_tokens      T >= 0.
+ *   ctas_unsplit    C >= 0, the unsplit kernel's CTA count for T tokens.
+ *   num_sms         S > 0.
+ *   opts            NULL or see tw_split_opts.
+ *   prefix_tokens   out: p.   suffix_tokens   out: T - p.   (host pointers)
+ *
+ * Pure host integer code: no CUDA call, no GPU needed.
+ * Errors: TW_ERR_INVALID_ARG (T < 0, C < 0, S <= 0, null output pointer,
+ * n_offsets < 0, offsets NULL with n_offsets > 0, a negative offset).
+ */
+int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_sms, const tw_split_opts* opts,
+                  int64_t* prefix_tokens, int64_t* suffix_tokens);
+
+/*
+ * tw_run_split -- the fused step over a token batch split in two, on two
+ * streams ([G] "Architectural Foundations of TokenWeave": the first chunk's
+ * fused step runs on a second stream while the first stream goes on; [W]
+ * "Fix one": prefix ops before suffix ops).
+ *
+ * Rows [0, prefix_tokens) run on stream_a and rows [prefix_tokens, T) on
+ * stream_b, each as tw_fused_reduce_residual_rmsnorm with the same sm_budget
+ * (so up to 2 * sm_budget SMs while both run). stream_b first waits for the
+ * work already queued on stream_a; on return stream_a is ordered after both
+ * halves. An empty half is not launched. The result is bitwise the same as
+ * the unsplit call. The call creates two CUDA events and destroys them before
+ * returning; it never destroys the streams. stream_a == stream_b is allowed
+ * (the halves then run in order).
+ *
+ * Arguments as for the fused call, plus prefix_tokens in [0, T].
+ */
+int tw_run_split(int64_t prefix_tokens, const void* const* partials, int N, void* residual,
+                 const void* gamma, float eps, int64_t T, int64_t H, void* out,
+                 tw_stream_t stream_a, tw_stream_t stream_b, int sm_budget);
+
+/* Text of a tw_status value (static storage; never NULL). */
+const char* tw_strerror(int status);
+
+/*
+ * tw_launch_shape -- the launch the fused call would make on the current
+ * device: grid (CTAs, = SMs used), threads per CTA, dynamic shared memory
+ * bytes and pipeline stages. Any output pointer may be NULL. Queries device
+ * attributes (TW_ERR_CUDA without a GPU). Validation as for the fused call.
+ */
+int tw_launch_shape(int64_t T, int64_t H, int N, int sm_budget, int* grid, int* threads,
+                    int* smem_bytes, int* stages);
+
+/*
+ * tw_device_status -- read, and optionally clear, the device-side error word
+ * that kernels set when a bounded wait gives up (a code other than 0 means
+ * the outputs of some call since the last reset are not valid). Synchronises
+ * the current device first. *code: 0 none; bit 0 a consumer gave up waiting
+ * for staged data; bit 1 the producer gave up waiting for a free stage; bit 2
+ * a final drain of in-flight copies gave up.
+ */
+int tw_device_status(int reset, int* code);
+
+/*
+ * tw_fused_debug_smid -- the fused call, additionally writing the %smid of
+ * each CTA to smid_out[blockIdx] (device int32 array with at least the
+ * grid's length, see tw_launch_shape). For checking that an sm_budget of k
+ * occupies at most k SMs.
+ */
+int tw_fused_debug_smid(const void* const* partials, int N, void* residual, const void* gamma,
+                        float eps, int64_t T, int64_t H, void* out, tw_stream_t stream,
+                        int sm_budget, int* smid_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TW_H */

@@ -1,0 +1,206 @@
+"""Python binding of libtw: fused reduce + residual + RMSNorm on one GB300.
+
+Argument marshalling only. Every step of the computation runs in libtw's CUDA
+kernels (``csrc/``) behind the C ABI declared in ``include/tw.h``; PyTorch
+supplies device memory and streams. There is no fallback: if ``libtw.so`` is
+missing or a call fails, an exception is raised.
+
+The functions carry the C names:
+
+    tw_fused_reduce_residual_rmsnorm(partials, residual, gamma, eps, out, stream=None, sm_budget=0)
+    tw_wave_split(num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS, min_split_tokens=1024)
+    tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a, stream_b, sm_budget=0)
+    tw_strerror(status)
+    tw_launch_shape(T, H, N, sm_budget=0)
+    tw_device_status(reset=True)
+    tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=None, sm_budget=0)
+"""
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtw.so")
+
+TW_OK = 0
+TW_ERR_INVALID_ARG = 1
+TW_ERR_ALIGN = 2
+TW_ERR_UNSUPPORTED = 3
+TW_ERR_CUDA = 4
+TW_ERR_DEVICE = 5
+TW_MAX_PARTIALS = 16
+TW_MAX_HIDDEN = 32768
+
+DEFAULT_OFFSETS = (0, 64, 128, 192, 256, 512)
+DEFAULT_MIN_SPLIT_TOKENS = 1024
+
+EXPORTED = ("tw_fused_reduce_residual_rmsnorm", "tw_wave_split", "tw_run_split", "tw_strerror",
+            "tw_launch_shape", "tw_device_status", "tw_fused_debug_smid")
+
+
+class TwError(RuntimeError):
+    """A libtw call returned a status other than TW_OK."""
+
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s" % (where, tw_strerror(status)))
+
+
+class _SplitOpts(ctypes.Structure):
+    _fields_ = [("offsets", ctypes.POINTER(ctypes.c_int)), ("n_offsets", ctypes.c_int),
+                ("min_split_tokens", ctypes.c_int)]
+
+
+_lib = None
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+
+def lib():
+    """The loaded libtw (ctypes.CDLL). Raises ImportError if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libtw.so is not built (%s); run `python -m reduce_rmsnorm_gb300.build`"
+                          % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    L.tw_fused_reduce_residual_rmsnorm.argtypes = [ctypes.POINTER(_vp), _int, _vp, _vp,
+                                                   ctypes.c_float, _i64, _i64, _vp, _vp, _int]
+    L.tw_fused_reduce_residual_rmsnorm.restype = _int
+    L.tw_fused_debug_smid.argtypes = [ctypes.POINTER(_vp), _int, _vp, _vp, ctypes.c_float, _i64,
+                                      _i64, _vp, _vp, _int, _vp]
+    L.tw_fused_debug_smid.restype = _int
+    L.tw_wave_split.argtypes = [_i64, _i64, _int, ctypes.POINTER(_SplitOpts),
+                                ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
+    L.tw_wave_split.restype = _int
+    L.tw_run_split.argtypes = [_i64, ctypes.POINTER(_vp), _int, _vp, _vp, ctypes.c_float, _i64,
+                               _i64, _vp, _vp, _vp, _int]
+    L.tw_run_split.restype = _int
+    L.tw_strerror.argtypes = [_int]
+    L.tw_strerror.restype = ctypes.c_char_p
+    L.tw_launch_shape.argtypes = [_i64, _i64, _int, _int] + [ctypes.POINTER(_int)] * 4
+    L.tw_launch_shape.restype = _int
+    L.tw_device_status.argtypes = [_int, ctypes.POINTER(_int)]
+    L.tw_device_status.restype = _int
+    _lib = L
+    return L
+
+
+def _check(status, where):
+    if status != TW_OK:
+        raise TwError(status, where)
+
+
+def tw_strerror(status):
+    return lib().tw_strerror(int(status)).decode()
+
+
+# ------------------------------------------------------------------ marshalling helpers
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _partials_array(partials):
+    """Host array of device pointers from a list of tensors or an [N, T, H] tensor."""
+    import torch
+    if isinstance(partials, torch.Tensor):
+        seq = [partials[i] for i in range(partials.shape[0])] if partials.dim() == 3 else [partials]
+    else:
+        seq = list(partials)
+    arr = (_vp * max(len(seq), 1))(*[t.data_ptr() for t in seq])
+    return arr, len(seq)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _shape(residual):
+    if residual.dim() != 2:
+        raise ValueError("residual must be [T, H]")
+    return int(residual.shape[0]), int(residual.shape[1])
+
+
+# ------------------------------------------------------------------ entry points
+
+
+def tw_fused_reduce_residual_rmsnorm(partials, residual, gamma, eps, out, stream=None, sm_budget=0):
+    """Fused step over rows [0, T): residual <- bf16(sum P + R); out <- RMSNorm.
+
+    partials: list of N bf16 [T, H] CUDA tensors or one [N, T, H] tensor;
+    residual (in/out), out: bf16 [T, H]; gamma: bf16 [H]. Shapes are read from
+    ``residual``; layout and error rules are those of the C call.
+    """
+    arr, n = _partials_array(partials)
+    T, H = _shape(residual)
+    st = lib().tw_fused_reduce_residual_rmsnorm(arr, n, _ptr(residual), _ptr(gamma), float(eps), T,
+                                                H, _ptr(out), _stream(stream), int(sm_budget))
+    _check(st, "tw_fused_reduce_residual_rmsnorm")
+
+
+def tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=None, sm_budget=0):
+    """The fused call that also records each CTA's SM id into ``smid_out`` (int32)."""
+    arr, n = _partials_array(partials)
+    T, H = _shape(residual)
+    st = lib().tw_fused_debug_smid(arr, n, _ptr(residual), _ptr(gamma), float(eps), T, H, _ptr(out),
+                                   _stream(stream), int(sm_budget), _ptr(smid_out))
+    _check(st, "tw_fused_debug_smid")
+
+
+def tw_wave_split(num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS,
+                  min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
+    """(prefix_tokens, suffix_tokens) of the wave-aware split.
+
+    offsets=None means every integer offset 0 .. half-1.
+    """
+    if offsets is None:
+        opts = _SplitOpts(None, 0, int(min_split_tokens))
+        keep = None
+    else:
+        keep = (ctypes.c_int * max(len(offsets), 1))(*[int(o) for o in offsets])
+        opts = _SplitOpts(keep, len(offsets), int(min_split_tokens))
+    p, s = _i64(), _i64()
+    st = lib().tw_wave_split(int(num_tokens), int(ctas_unsplit), int(num_sms), ctypes.byref(opts),
+                             ctypes.byref(p), ctypes.byref(s))
+    del keep
+    _check(st, "tw_wave_split")
+    return p.value, s.value
+
+
+def tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a=None, stream_b=None,
+                 sm_budget=0):
+    """Rows [0, prefix) on stream_a, [prefix, T) on stream_b; stream_a joins both."""
+    arr, n = _partials_array(partials)
+    T, H = _shape(residual)
+    st = lib().tw_run_split(int(prefix_tokens), arr, n, _ptr(residual), _ptr(gamma), float(eps), T,
+                            H, _ptr(out), _stream(stream_a), _stream(stream_b), int(sm_budget))
+    _check(st, "tw_run_split")
+
+
+def tw_launch_shape(T, H, N, sm_budget=0):
+    """dict(grid, threads, smem_bytes, stages) of the launch on the current device."""
+    g, t, m, s = _int(), _int(), _int(), _int()
+    st = lib().tw_launch_shape(int(T), int(H), int(N), int(sm_budget), ctypes.byref(g),
+                               ctypes.byref(t), ctypes.byref(m), ctypes.byref(s))
+    _check(st, "tw_launch_shape")
+    return dict(grid=g.value, threads=t.value, smem_bytes=m.value, stages=s.value)
+
+
+def tw_device_status(reset=True):
+    """The device error word (0 = no kernel gave up a wait); synchronises."""
+    code = _int()
+    _check(lib().tw_device_status(1 if reset else 0, ctypes.byref(code)), "tw_device_status")
+    return code.value
+
+
+def bytes_per_call(T, H, N):
+    """Algorithmic HBM bytes of one fused call: read N partials and the
+    residual, write the residual and the output, read gamma once."""
+    return (N + 3) * T * H * 2 + H * 2

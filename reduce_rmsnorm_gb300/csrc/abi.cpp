@@ -1,0 +1,184 @@
+// C-ABI entry points of libtw (declared and documented in include/tw.h).
+// Validation happens here, before any CUDA call; kernels are in fused_kernel.cu.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "tw.h"
+#include "tw_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, const void* b, int64_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  const uintptr_t n = static_cast<uintptr_t>(bytes);
+  return x < y + n && y < x + n;
+}
+
+// Checks that do not look at pointers (shared by the launch-shape query).
+int validate_shape(int N, float eps, int64_t T, int64_t H, int sm_budget) {
+  if (N < 1 || N > TW_MAX_PARTIALS) return TW_ERR_INVALID_ARG;
+  if (T < 0 || H <= 0) return TW_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return TW_ERR_INVALID_ARG;
+  if (sm_budget < 0) return TW_ERR_INVALID_ARG;
+  if (H % 8 != 0) return TW_ERR_ALIGN;
+  if (H > TW_MAX_HIDDEN) return TW_ERR_UNSUPPORTED;
+  if (T > (INT64_MAX / 4) / H) return TW_ERR_INVALID_ARG;  // T * H * 2 bytes must not overflow
+  return TW_OK;
+}
+
+// Full validation of one fused call over rows [0, T); fills the kernel args.
+int validate(const void* const* partials, int N, void* residual, const void* gamma, float eps,
+             int64_t T, int64_t H, void* out, int sm_budget, tw::FusedArgs* a) {
+  int st = validate_shape(N, eps, T, H, sm_budget);
+  if (st != TW_OK) return st;
+  if (T == 0) return TW_OK;
+  if (!partials || !residual || !gamma || !out) return TW_ERR_INVALID_ARG;
+  for (int r = 0; r < N; ++r)
+    if (!partials[r]) return TW_ERR_INVALID_ARG;
+  for (int r = 0; r < N; ++r)
+    if (!aligned16(partials[r])) return TW_ERR_ALIGN;
+  if (!aligned16(residual) || !aligned16(gamma) || !aligned16(out)) return TW_ERR_ALIGN;
+  const int64_t bytes = T * H * 2;
+  // The two written tensors may overlap nothing else (inputs may alias each other).
+  if (overlap(residual, out, bytes)) return TW_ERR_INVALID_ARG;
+  for (void* w : {residual, out}) {
+    if (overlap(w, gamma, H * 2)) return TW_ERR_INVALID_ARG;
+    for (int r = 0; r < N; ++r)
+      if (overlap(w, partials[r], bytes)) return TW_ERR_INVALID_ARG;
+  }
+  for (int r = 0; r < N; ++r) a->partials[r] = partials[r];
+  a->n = N;
+  a->residual = residual;
+  a->gamma = gamma;
+  a->out = out;
+  a->eps = eps;
+  a->rows = T;
+  a->hidden = H;
+  return TW_OK;
+}
+
+// Rows [row0, row0 + rows) of a validated call.
+tw::FusedArgs slice(const tw::FusedArgs& a, int64_t row0, int64_t rows) {
+  tw::FusedArgs s = a;
+  const int64_t off = row0 * a.hidden * 2;
+  for (int r = 0; r < a.n; ++r) s.partials[r] = static_cast<const char*>(a.partials[r]) + off;
+  s.residual = static_cast<char*>(a.residual) + off;
+  s.out = static_cast<char*>(a.out) + off;
+  s.rows = rows;
+  return s;
+}
+
+}  // namespace
+
+extern "C" int tw_fused_reduce_residual_rmsnorm(const void* const* partials, int N, void* residual,
+                                                const void* gamma, float eps, int64_t T, int64_t H,
+                                                void* out, tw_stream_t stream, int sm_budget) {
+  try {
+    tw::FusedArgs a;
+    const int st = validate(partials, N, residual, gamma, eps, T, H, out, sm_budget, &a);
+    if (st != TW_OK || T == 0) return st;
+    return tw::launch_fused(a, reinterpret_cast<cudaStream_t>(stream), sm_budget, nullptr);
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
+extern "C" int tw_fused_debug_smid(const void* const* partials, int N, void* residual,
+                                   const void* gamma, float eps, int64_t T, int64_t H, void* out,
+                                   tw_stream_t stream, int sm_budget, int* smid_out) {
+  try {
+    if (!smid_out) return TW_ERR_INVALID_ARG;
+    tw::FusedArgs a;
+    const int st = validate(partials, N, residual, gamma, eps, T, H, out, sm_budget, &a);
+    if (st != TW_OK || T == 0) return st;
+    return tw::launch_fused(a, reinterpret_cast<cudaStream_t>(stream), sm_budget, smid_out);
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
+extern "C" int tw_run_split(int64_t prefix_tokens, const void* const* partials, int N,
+                            void* residual, const void* gamma, float eps, int64_t T, int64_t H,
+                            void* out, tw_stream_t stream_a, tw_stream_t stream_b, int sm_budget) {
+  try {
+    tw::FusedArgs a;
+    int st = validate(partials, N, residual, gamma, eps, T, H, out, sm_budget, &a);
+    if (st != TW_OK) return st;
+    if (prefix_tokens < 0 || prefix_tokens > T) return TW_ERR_INVALID_ARG;
+    if (T == 0) return TW_OK;
+    cudaStream_t sa = reinterpret_cast<cudaStream_t>(stream_a);
+    cudaStream_t sb = reinterpret_cast<cudaStream_t>(stream_b);
+    const int64_t suffix = T - prefix_tokens;
+    if (suffix == 0 || sa == sb) {
+      if (prefix_tokens > 0 &&
+          (st = tw::launch_fused(slice(a, 0, prefix_tokens), sa, sm_budget, nullptr)) != TW_OK)
+        return st;
+      if (suffix > 0)
+        return tw::launch_fused(slice(a, prefix_tokens, suffix), sa, sm_budget, nullptr);
+      return TW_OK;
+    }
+    cudaEvent_t fork = nullptr, join = nullptr;
+    if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return TW_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventDestroy(fork);
+      return TW_ERR_CUDA;
+    }
+    st = TW_OK;
+    if (cudaEventRecord(fork, sa) != cudaSuccess || cudaStreamWaitEvent(sb, fork, 0) != cudaSuccess)
+      st = TW_ERR_CUDA;
+    if (st == TW_OK && prefix_tokens > 0)
+      st = tw::launch_fused(slice(a, 0, prefix_tokens), sa, sm_budget, nullptr);
+    if (st == TW_OK) st = tw::launch_fused(slice(a, prefix_tokens, suffix), sb, sm_budget, nullptr);
+    if (st == TW_OK &&
+        (cudaEventRecord(join, sb) != cudaSuccess || cudaStreamWaitEvent(sa, join, 0) != cudaSuccess))
+      st = TW_ERR_CUDA;
+    cudaEventDestroy(fork);
+    cudaEventDestroy(join);
+    return st;
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
+extern "C" int tw_launch_shape(int64_t T, int64_t H, int N, int sm_budget, int* grid, int* threads,
+                               int* smem_bytes, int* stages) {
+  try {
+    const int st = validate_shape(N, 0.0f, T, H, sm_budget);
+    if (st != TW_OK) return st;
+    tw::LaunchShape s;
+    const int q = tw::plan_launch(T, H, N, sm_budget, &s);
+    if (q != TW_OK) return q;
+    if (grid) *grid = s.grid;
+    if (threads) *threads = s.threads;
+    if (smem_bytes) *smem_bytes = s.smem_bytes;
+    if (stages) *stages = s.stages;
+    return TW_OK;
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
+extern "C" int tw_device_status(int reset, int* code) {
+  try {
+    if (!code) return TW_ERR_INVALID_ARG;
+    return tw::read_device_error(reset, code);
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
+extern "C" const char* tw_strerror(int status) {
+  switch (status) {
+    case TW_OK: return "TW_OK: success";
+    case TW_ERR_INVALID_ARG: return "TW_ERR_INVALID_ARG: invalid argument";
+    case TW_ERR_ALIGN: return "TW_ERR_ALIGN: H must be a multiple of 8 and pointers 16-byte aligned";
+    case TW_ERR_UNSUPPORTED: return "TW_ERR_UNSUPPORTED: hidden size above TW_MAX_HIDDEN";
+    case TW_ERR_CUDA: return "TW_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case TW_ERR_DEVICE: return "TW_ERR_DEVICE: a kernel gave up on a bounded wait";
+    default: return "unknown tw_status";
+  }
+}

@@ -1,0 +1,456 @@
+// Fused reduce + residual + RMSNorm kernel for sm_103a.
+//
+// [W] = "TokenWeave: Why Hiding Tensor-Parallel Communication Needs Wave
+// Arithmetic, Not Finer Tiles", section "Fix two: RMSNorm was never
+// insignificant": per CTA, load-and-reduce the ranks' vectors, add the
+// residual in the same pass, take the sum of squares on the register-resident
+// result (no HBM re-read), scale by rsqrt(variance / hidden_size + eps) and the
+// weight, store once. On one GPU the ranks' contributions are N local buffers.
+//
+// GB300 design (not the pages' multimem kernel, which targets NVSwitch):
+//   * Persistent: one CTA per SM (it asks for ~216 KB of shared memory, so no
+//     second CTA of this kernel fits), each owning a contiguous range of token
+//     rows ([W]'s tokens_per_cta = ceil(num_tokens / gridDim.x), balanced).
+//     The grid size is the SM budget.
+//   * Warp-specialised: one producer lane streams each row, in 4 KiB chunks of
+//     every source (N partials + residual), from HBM into a ring of shared
+//     memory stages with 1-D TMA bulk copies (cp.async.bulk, mbarrier
+//     completion, L2 evict-first). Eight consumer warps read a chunk (one
+//     16-byte vector per thread per source), sum in fp32 in rank order, add
+//     the residual, store the updated residual, and keep z in registers.
+//   * After a row's last chunk: warp xor-shuffle sum of squares, a fixed-order
+//     combine of the 8 warp sums, rsqrtf, and Y = (z * r) * gamma stored with
+//     16-byte stores. The per-row arithmetic depends only on H, so every grid
+//     size (SM budget), split and shard gives bitwise the same rows.
+//   * Every wait on an mbarrier is bounded (time and iterations); on giving up
+//     the CTA sets a device error word and finishes without further waits.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "tw_internal.h"
+
+namespace tw {
+
+// Device-side error word (bit 0: consumer wait, bit 1: producer wait,
+// bit 2: final drain). Read and cleared by read_device_error().
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kChunkVec = kConsumerThreads;      // 16-byte vectors per source per chunk
+constexpr int kChunkBytes = kChunkVec * 16;      // 4 KiB
+constexpr int kMaxStages = 32;
+constexpr int kConsumerBarrierId = 1;            // named barrier of the consumer warps
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // give up after 2 s
+constexpr uint32_t kWaitLimitPolls = 1u << 26;
+constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s per stage
+
+struct Params {
+  const uint4* partials[TW_MAX_PARTIALS];
+  const uint4* gamma;
+  uint4* residual;
+  uint4* out;
+  int* smid_out;
+  long long rows;
+  int vec_per_row;  // H / 8
+  int n_partials;
+  int chunks;       // ceil(vec_per_row / kChunkVec)
+  int stages;
+  float eps;
+  float hidden;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D TMA bulk copy global -> shared, completing `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void consumer_barrier() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrierId), "n"(kConsumerThreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t id;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
+  return id;
+}
+
+// Wait for the phase of the given parity of *bar to complete. Bounded: gives
+// up after kWaitLimitNs or kWaitLimitPolls polls, then sets *abort and the
+// device error word. Returns false at once while *abort is set.
+__device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned code) {
+  if (*abort) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t i = 1; i < kWaitLimitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0u) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  *abort = 1;
+  atomicOr(&g_device_error, code);
+  return false;
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight copies).
+__device__ bool drain_phase(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t i = 0; i < kWaitLimitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && global_timer_ns() - t0 > kDrainLimitNs) break;
+  }
+  atomicOr(&g_device_error, 4u);
+  return false;
+}
+
+// ------------------------------------------------------------------ bf16 x 8
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void load8(const uint4 q, float a[8]) {
+  a[0] = bf16_lo(q.x); a[1] = bf16_hi(q.x);
+  a[2] = bf16_lo(q.y); a[3] = bf16_hi(q.y);
+  a[4] = bf16_lo(q.z); a[5] = bf16_hi(q.z);
+  a[6] = bf16_lo(q.w); a[7] = bf16_hi(q.w);
+}
+
+__device__ __forceinline__ void add8(const uint4 q, float a[8]) {
+  a[0] += bf16_lo(q.x); a[1] += bf16_hi(q.x);
+  a[2] += bf16_lo(q.y); a[3] += bf16_hi(q.y);
+  a[4] += bf16_lo(q.z); a[5] += bf16_hi(q.z);
+  a[6] += bf16_lo(q.w); a[7] += bf16_hi(q.w);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8(const float a[8]) {
+  return make_uint4(pack2(a[0], a[1]), pack2(a[2], a[3]), pack2(a[4], a[5]), pack2(a[6], a[7]));
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ float warp_ss[2][kConsumerWarps];
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const long long grid = gridDim.x;
+  const long long row0 = static_cast<long long>(blockIdx.x) * p.rows / grid;
+  const long long row1 = static_cast<long long>(blockIdx.x + 1) * p.rows / grid;
+  const int n = p.n_partials;
+  const int vpr = p.vec_per_row;
+  const int chunks = p.chunks;
+  const int stages = p.stages;
+  const uint32_t stage_bytes = static_cast<uint32_t>(n + 1) * kChunkBytes;
+
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+    if (p.smid_out) p.smid_out[blockIdx.x] = static_cast<int>(sm_id());
+  }
+  __syncthreads();
+  volatile int* abort = &abort_flag;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: one lane streams (row, chunk) items into the ring
+    if (lane != 0) return;
+    const uint64_t policy = l2_evict_first_policy();
+    const long long items = (row1 - row0) * chunks;
+    long long issued = 0;
+    long long row = row0;
+    int chunk = 0, s = 0;
+    uint32_t round_parity = 0;  // parity of the current pass over the ring
+    bool first_pass = true;
+    for (long long it = 0; it < items; ++it) {
+      if (!first_pass && !wait_phase(&empty_bar[s], round_parity ^ 1u, abort, 2u)) break;
+      const int v0 = chunk * kChunkVec;
+      const int nvec = min(kChunkVec, vpr - v0);
+      const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
+      mbar_arrive_expect_tx(&full_bar[s], bytes * static_cast<uint32_t>(n + 1));
+      unsigned char* dst = ring + static_cast<size_t>(s) * stage_bytes;
+      const long long off = row * vpr + v0;
+      for (int r = 0; r < n; ++r)
+        bulk_load(dst + r * kChunkBytes, p.partials[r] + off, bytes, &full_bar[s], policy);
+      bulk_load(dst + n * kChunkBytes, p.residual + off, bytes, &full_bar[s], policy);
+      ++issued;
+      if (++chunk == chunks) { chunk = 0; ++row; }
+      if (++s == stages) { s = 0; round_parity ^= 1u; first_pass = false; }
+    }
+    if (*abort) {
+      // Let every copy this CTA issued land before the CTA exits: the last
+      // item issued on each stage completes after all earlier ones there.
+      const long long last = issued - 1;
+      for (int st = 0; st < stages && st <= last; ++st) {
+        const long long it_last = last - ((last - st) % stages);
+        drain_phase(&full_bar[st], static_cast<uint32_t>((it_last / stages) & 1));
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers: 8 warps, thread t owns vectors t, t+256, ... of each row
+  const int t = tid;
+  const uint32_t ring_base = smem_addr(ring) + static_cast<uint32_t>(t) * 16u;
+  int s = 0;
+  uint32_t parity = 0;
+  float z[KMAX][8];
+  for (long long row = row0; row < row1; ++row) {
+    float ss = 0.0f;
+    uint4* res_row = p.residual + row * vpr;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (k < chunks) {
+        const int v = k * kChunkVec + t;
+        const bool active = v < vpr;
+        wait_phase(&full_bar[s], parity, abort, 1u);
+        float a[8];
+        if (active) {
+          const uint32_t src = ring_base + static_cast<uint32_t>(s) * stage_bytes;
+          load8(lds128(src), a);
+          for (int r = 1; r < n; ++r) add8(lds128(src + r * kChunkBytes), a);
+          add8(lds128(src + n * kChunkBytes), a);  // residual last
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (active) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            z[k][i] = a[i];
+            ss = fmaf(a[i], a[i], ss);
+          }
+          res_row[v] = pack8(a);
+        }
+        if (++s == stages) { s = 0; parity ^= 1u; }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const int buf = static_cast<int>((row - row0) & 1);
+    if (lane == 0) warp_ss[buf][warp] = ss;
+    consumer_barrier();
+    float total = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) total += warp_ss[buf][w];
+    const float rs = rsqrtf(total / p.hidden + p.eps);
+    uint4* out_row = p.out + row * vpr;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      const int v = k * kChunkVec + t;
+      if (k < chunks && v < vpr) {
+        float g[8], y[8];
+        load8(__ldg(p.gamma + v), g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = (z[k][i] * rs) * g[i];
+        out_row[v] = pack8(y);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+constexpr int kMaxDevices = 64;
+constexpr int kStaticSmemReserve = 2048;  // barriers, warp sums, flag, slack
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int smem_optin = 0;
+  bool attr_done[5] = {false, false, false, false, false};
+};
+
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+int kmax_index(int chunks) {
+  if (chunks <= 1) return 0;
+  if (chunks <= 2) return 1;
+  if (chunks <= 4) return 2;
+  if (chunks <= 8) return 3;
+  return 4;
+}
+
+using KernelFn = void (*)(Params);
+const KernelFn kKernels[5] = {fused_kernel<1>, fused_kernel<2>, fused_kernel<4>, fused_kernel<8>,
+                              fused_kernel<16>};
+
+int device_info(DeviceInfo** out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TW_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return TW_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      return TW_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  *dev_out = dev;
+  return TW_OK;
+}
+
+}  // namespace
+
+int plan_launch(int64_t rows, int64_t hidden, int n, int sm_budget, LaunchShape* shape) {
+  DeviceInfo* d = nullptr;
+  int dev = 0;
+  const int st = device_info(&d, &dev);
+  if (st != TW_OK) return st;
+  const int vpr = static_cast<int>(hidden / 8);
+  const int chunks = (vpr + kChunkVec - 1) / kChunkVec;
+  const int stage_bytes = (n + 1) * kChunkBytes;
+  int stages = (d->smem_optin - kStaticSmemReserve) / stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return TW_ERR_UNSUPPORTED;
+  int grid = d->sms;
+  if (sm_budget > 0 && sm_budget < grid) grid = sm_budget;
+  if (rows < grid) grid = static_cast<int>(rows);
+  shape->grid = grid;
+  shape->threads = kThreads;
+  shape->smem_bytes = stages * stage_bytes;
+  shape->stages = stages;
+  shape->kmax = 1 << kmax_index(chunks);
+  return TW_OK;
+}
+
+int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* smid_out) {
+  LaunchShape shape;
+  int st = plan_launch(a.rows, a.hidden, a.n, sm_budget, &shape);
+  if (st != TW_OK) return st;
+  if (shape.grid <= 0) return TW_OK;
+
+  Params p;
+  for (int r = 0; r < TW_MAX_PARTIALS; ++r)
+    p.partials[r] = r < a.n ? static_cast<const uint4*>(a.partials[r]) : nullptr;
+  p.gamma = static_cast<const uint4*>(a.gamma);
+  p.residual = static_cast<uint4*>(a.residual);
+  p.out = static_cast<uint4*>(a.out);
+  p.smid_out = smid_out;
+  p.rows = a.rows;
+  p.vec_per_row = static_cast<int>(a.hidden / 8);
+  p.n_partials = a.n;
+  p.chunks = (p.vec_per_row + kChunkVec - 1) / kChunkVec;
+  p.stages = shape.stages;
+  p.eps = a.eps;
+  p.hidden = static_cast<float>(a.hidden);
+
+  const int ki = kmax_index(p.chunks);
+  DeviceInfo* d = nullptr;
+  int dev = 0;
+  st = device_info(&d, &dev);
+  if (st != TW_OK) return st;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!d->attr_done[ki]) {
+      const int max_dyn = d->smem_optin - kStaticSmemReserve;
+      if (cudaFuncSetAttribute(kKernels[ki], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               max_dyn) != cudaSuccess)
+        return TW_ERR_CUDA;
+      d->attr_done[ki] = true;
+    }
+  }
+  kKernels[ki]<<<shape.grid, kThreads, shape.smem_bytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? TW_OK : TW_ERR_CUDA;
+}
+
+int read_device_error(int reset, int* code) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return TW_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return TW_ERR_CUDA;
+  if (reset) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return TW_ERR_CUDA;
+  }
+  if (code) *code = static_cast<int>(v);
+  return TW_OK;
+}
+
+}  // namespace tw

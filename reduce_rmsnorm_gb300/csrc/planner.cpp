@@ -1,0 +1,90 @@
+// Wave-aware prefix/suffix token split (pure host integer code, no CUDA).
+//
+// [W] = "TokenWeave: Why Hiding Tensor-Parallel Communication Needs Wave
+// Arithmetic, Not Finer Tiles". "The overlap trap": a c-CTA kernel on S SMs
+// runs in ceil(c/S) waves. "Fix one: split at wave boundaries, unequally":
+// split the batch exactly twice, prefix = half + offset, suffix = half -
+// offset, offsets from {0, 64, 128, 192, 256, 512} below half, keeping the
+// waves of the two pieces within the unsplit count; one-wave kernels and
+// batches under the 1K-token threshold are not split. The worked example
+// (132 / 168 of 300 CTAs) puts the smaller piece first, so offsets are tried
+// with both signs, smallest |offset| first and the smaller prefix on a tie.
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+#include "tw.h"
+
+namespace {
+
+const int kDefaultOffsets[] = {0, 64, 128, 192, 256, 512};
+const int kDefaultMinSplitTokens = 1024;
+
+int64_t ceil_div(int64_t a, int64_t b) { return a / b + (a % b != 0); }  // a >= 0, b > 0
+
+// CTAs of a t-token piece of a T-token, C-CTA kernel: ceil(t * C / T).
+int64_t piece_ctas(int64_t t, int64_t T, int64_t C) {
+  const __int128 n = static_cast<__int128>(t) * C;
+  return static_cast<int64_t>(n / T + (n % T != 0));
+}
+
+}  // namespace
+
+extern "C" int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_sms,
+                             const tw_split_opts* opts, int64_t* prefix_tokens,
+                             int64_t* suffix_tokens) {
+  if (!prefix_tokens || !suffix_tokens) return TW_ERR_INVALID_ARG;
+  if (num_tokens < 0 || ctas_unsplit < 0 || num_sms <= 0) return TW_ERR_INVALID_ARG;
+
+  bool every_offset = false;
+  std::vector<int64_t> offsets(std::begin(kDefaultOffsets), std::end(kDefaultOffsets));
+  int64_t min_split = kDefaultMinSplitTokens;
+  if (opts) {
+    if (opts->n_offsets < 0) return TW_ERR_INVALID_ARG;
+    if (!opts->offsets && opts->n_offsets > 0) return TW_ERR_INVALID_ARG;
+    if (!opts->offsets) {
+      every_offset = true;
+    } else {
+      offsets.assign(opts->offsets, opts->offsets + opts->n_offsets);
+      for (int64_t o : offsets)
+        if (o < 0) return TW_ERR_INVALID_ARG;
+    }
+    min_split = opts->min_split_tokens;
+  }
+
+  const int64_t T = num_tokens, C = ctas_unsplit, S = num_sms;
+  *prefix_tokens = T;
+  *suffix_tokens = 0;
+  if (T == 0) return TW_OK;
+  const int64_t unsplit_waves = ceil_div(C, S);
+  if (T < min_split || unsplit_waves <= 1) return TW_OK;
+
+  const int64_t half = T / 2;
+  auto admissible = [&](int64_t p) {
+    return ceil_div(piece_ctas(p, T, C), S) + ceil_div(piece_ctas(T - p, T, C), S) <= unsplit_waves;
+  };
+  auto try_offset = [&](int64_t off) {
+    if (admissible(half - off)) {
+      *prefix_tokens = half - off;
+    } else if (off > 0 && admissible(half + off)) {
+      *prefix_tokens = half + off;
+    } else {
+      return false;
+    }
+    *suffix_tokens = T - *prefix_tokens;
+    return true;
+  };
+
+  if (every_offset) {
+    for (int64_t off = 0; off < half; ++off)
+      if (try_offset(off)) return TW_OK;
+    return TW_OK;
+  }
+  std::sort(offsets.begin(), offsets.end());
+  offsets.erase(std::unique(offsets.begin(), offsets.end()), offsets.end());
+  for (int64_t off : offsets) {
+    if (off >= half) break;
+    if (try_offset(off)) return TW_OK;
+  }
+  return TW_OK;
+}

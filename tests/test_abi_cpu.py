@@ -1,0 +1,229 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol the header
+declares, its host-only planner equals the brute-force oracle, and argument
+validation returns status codes before any CUDA call (no GPU is touched:
+pointers here are fake addresses that validation never dereferences)."""
+
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import reduce_rmsnorm_gb300 as tw
+from oracle import planner as oplanner
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from reduce_rmsnorm_gb300 import build
+    build.build()
+    return tw.lib()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "tw.h")).read()
+    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(tw_\w+)\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    syms = _declared_symbols()
+    for name in ("tw_fused_reduce_residual_rmsnorm", "tw_wave_split", "tw_run_split", "tw_strerror"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_symbols():
+        assert hasattr(L, name), name
+    assert set(_declared_symbols()) <= set(tw.EXPORTED) | set()
+    for name in tw.EXPORTED:
+        assert name in _declared_symbols(), name
+
+
+def test_strerror(L):
+    for code in range(6):
+        assert tw.tw_strerror(code).startswith("TW_")
+    assert "unknown" in tw.tw_strerror(99)
+
+
+# ------------------------------------------------------------------ planner (pure host)
+
+
+def _golden_planner_cases():
+    path = os.path.join(ROOT, "tests", "golden", "planner_pins.txt")
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        lhs, rhs = line.split("->")
+        T, C, S, offs, mins = lhs.split()
+        p, s = rhs.split()
+        yield int(T), int(C), int(S), (None if offs == "all" else tw.DEFAULT_OFFSETS), int(mins), int(p), int(s)
+
+
+def test_planner_golden(L):
+    for T, C, S, offs, mins, p, s in _golden_planner_cases():
+        assert tw.tw_wave_split(T, C, S, offs, mins) == (p, s), (T, C, S)
+
+
+def test_planner_configs_at_148_sms(L):
+    # Token counts of the split workload; C = ceil(T/128) * (8192/128) / 8.
+    for T, want in [(1024, (1024, 0)), (2048, (2048, 0)), (4096, (2048, 2048)), (8192, (4096, 4096))]:
+        C = math.ceil(T / 128) * (8192 // 128) // 8
+        assert tw.tw_wave_split(T, C, 148) == want
+        assert oplanner.wave_split(T, C, 148) == want
+
+
+def test_planner_exhaustive_small_every_offset(L):
+    """Every (T, C, S) with T <= 40, C <= 40, S <= 20, every integer offset, no threshold."""
+    n = 0
+    for T in range(0, 41):
+        for C in range(0, 41):
+            for S in range(1, 21):
+                want = oplanner.wave_split(T, C, S, None, 0)
+                assert tw.tw_wave_split(T, C, S, None, 0) == want, (T, C, S)
+                n += 1
+    assert n == 41 * 41 * 20
+
+
+def test_planner_random_default_grid(L):
+    rng = np.random.Generator(np.random.PCG64(2024))
+    for _ in range(600):
+        T = int(rng.integers(0, 6000))
+        C = int(rng.integers(0, 1200))
+        S = int(rng.integers(1, 300))
+        mins = int(rng.choice([0, 512, 1024, 4096]))
+        assert tw.tw_wave_split(T, C, S, tw.DEFAULT_OFFSETS, mins) == \
+            oplanner.wave_split(T, C, S, tw.DEFAULT_OFFSETS, mins), (T, C, S, mins)
+
+
+def test_planner_custom_offsets_unsorted_duplicates(L):
+    rng = np.random.Generator(np.random.PCG64(99))
+    for _ in range(200):
+        offs = [int(x) for x in rng.integers(0, 700, size=int(rng.integers(1, 8)))]
+        offs += offs[:2]
+        T = int(rng.integers(1024, 5000))
+        C = int(rng.integers(1, 900))
+        S = int(rng.integers(1, 200))
+        assert tw.tw_wave_split(T, C, S, offs, 1024) == oplanner.wave_split(T, C, S, offs, 1024)
+
+
+def test_planner_rejects_bad_args(L):
+    bad = [(-1, 5, 4, tw.DEFAULT_OFFSETS), (10, -1, 4, tw.DEFAULT_OFFSETS),
+           (10, 5, 0, tw.DEFAULT_OFFSETS), (2048, 500, 100, (0, -64))]
+    for T, C, S, offs in bad:
+        with pytest.raises(tw.TwError) as e:
+            tw.tw_wave_split(T, C, S, offs)
+        assert e.value.status == tw.TW_ERR_INVALID_ARG
+    p = ctypes.c_int64()
+    assert L.tw_wave_split(10, 5, 4, None, None, ctypes.byref(p)) == tw.TW_ERR_INVALID_ARG
+    opts = tw._SplitOpts(None, 3, 0)  # NULL offsets with a positive count
+    assert L.tw_wave_split(10, 5, 4, ctypes.byref(opts), ctypes.byref(p),
+                           ctypes.byref(ctypes.c_int64())) == tw.TW_ERR_INVALID_ARG
+
+
+def test_planner_large_values_no_overflow(L):
+    T = 1 << 40
+    C = 1 << 30
+    p, s = tw.tw_wave_split(T, C, 148)
+    assert p + s == T
+
+
+# ------------------------------------------------------------------ fused-call validation
+
+
+BASE = 0x7F0000000000  # fake device addresses; validation never dereferences them
+
+
+def _fused(L, N=2, T=4, H=16, eps=1e-5, sm_budget=0, partials=None, residual=None, gamma=None,
+           out=None):
+    span = max(T * H * 2, 16) + 4096
+    if partials is None:
+        partials = [BASE + (r + 1) * (1 << 24) for r in range(N)]
+    arr = (ctypes.c_void_p * max(len(partials), 1))(*partials)
+    residual = BASE + (40 << 24) if residual is None else residual
+    gamma = BASE + (41 << 24) if gamma is None else gamma
+    out = BASE + (42 << 24) if out is None else out
+    del span
+    return L.tw_fused_reduce_residual_rmsnorm(arr, N, residual, gamma, ctypes.c_float(eps), T, H,
+                                              out, None, sm_budget)
+
+
+def test_validation_scalar_args(L):
+    assert _fused(L, N=0) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, N=17, partials=[BASE + (r + 1) * (1 << 24) for r in range(17)]) == \
+        tw.TW_ERR_INVALID_ARG
+    assert _fused(L, T=-1) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, H=0) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, H=12) == tw.TW_ERR_ALIGN
+    assert _fused(L, H=tw.TW_MAX_HIDDEN + 8) == tw.TW_ERR_UNSUPPORTED
+    assert _fused(L, eps=-1e-5) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, eps=float("nan")) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, eps=float("inf")) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, sm_budget=-1) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, T=1 << 60, H=8192) == tw.TW_ERR_INVALID_ARG
+
+
+def test_validation_empty_batch_is_a_noop(L):
+    # T == 0 returns before looking at pointers or calling CUDA.
+    assert _fused(L, T=0, partials=[0, 0], residual=0, gamma=0, out=0) == tw.TW_OK
+    arr = (ctypes.c_void_p * 2)(0, 0)
+    assert L.tw_run_split(0, arr, 2, None, None, ctypes.c_float(1e-5), 0, 16, None, None, None,
+                          0) == tw.TW_OK
+
+
+def test_validation_pointers(L):
+    assert _fused(L, partials=[BASE + (1 << 24), 0]) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, residual=0) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, gamma=0) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, out=0) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, partials=[BASE + (1 << 24) + 8, BASE + (2 << 24)]) == tw.TW_ERR_ALIGN
+    assert _fused(L, residual=BASE + (40 << 24) + 4) == tw.TW_ERR_ALIGN
+    assert _fused(L, gamma=BASE + (41 << 24) + 2) == tw.TW_ERR_ALIGN
+    assert _fused(L, out=BASE + (42 << 24) + 8) == tw.TW_ERR_ALIGN
+
+
+def test_validation_overlaps(L):
+    T, H = 4, 16
+    r = BASE + (40 << 24)
+    # out overlapping the residual (by one row) is rejected
+    assert _fused(L, T=T, H=H, residual=r, out=r + H * 2) == tw.TW_ERR_INVALID_ARG
+    # out adjacent to the residual is fine up to the CUDA call; here check only
+    # that a written tensor overlapping a partial or gamma is rejected
+    assert _fused(L, T=T, H=H, out=BASE + (1 << 24) + 16) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, T=T, H=H, residual=BASE + (41 << 24) - 16) == tw.TW_ERR_INVALID_ARG
+    # partials aliasing one another is allowed by validation (reads only):
+    # the call gets past validation and fails only at the first CUDA call
+    # when there is no GPU, or launches when there is one -- not run here.
+
+
+def test_run_split_prefix_range(L):
+    arr = (ctypes.c_void_p * 2)(BASE + (1 << 24), BASE + (2 << 24))
+    for prefix in (-1, 5):
+        st = L.tw_run_split(prefix, arr, 2, BASE + (40 << 24), BASE + (41 << 24),
+                            ctypes.c_float(1e-5), 4, 16, BASE + (42 << 24), None, None, 0)
+        assert st == tw.TW_ERR_INVALID_ARG
+
+
+def test_launch_shape_validates_before_device_query(L):
+    g = ctypes.c_int()
+    assert L.tw_launch_shape(4, 12, 2, 0, ctypes.byref(g), None, None, None) == tw.TW_ERR_ALIGN
+    assert L.tw_launch_shape(4, 16, 0, 0, ctypes.byref(g), None, None, None) == \
+        tw.TW_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(tw, "_lib", None)
+    monkeypatch.setattr(tw, "LIB_PATH", "/nonexistent/libtw.so")
+    with pytest.raises(ImportError):
+        tw.lib()
+
+
+def test_bytes_formula():
+    # (N+3) * T * H * 2 + H * 2 : the Llama-3.3-70B layer shape
+    assert tw.bytes_per_call(1024, 8192, 8) == 184_565_760
+    assert tw.bytes_per_call(128, 4096, 2) == 5_251_072
+    assert tw.bytes_per_call(8192, 16384, 8) == 2_952_822_784

@@ -1,0 +1,289 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, and the
+bitwise invariants of the launch shape: SM budget, token shards, two-stream
+split, repeat runs. Needs a GPU.
+
+Pages cited: [W] "TokenWeave: Why Hiding Tensor-Parallel Communication Needs
+Wave Arithmetic, Not Finer Tiles"."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import reduce_rmsnorm_gb300 as tw
+import synth
+from oracle import planner as oplanner
+from parity import check_rows, to_gpu
+
+pytestmark = pytest.mark.gpu
+
+EPS = synth.EPS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from reduce_rmsnorm_gb300 import build
+    build.build()
+    tw.lib()
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    tw.tw_device_status(reset=True)
+    yield
+    assert tw.tw_device_status(reset=True) == 0, "a kernel gave up on a bounded wait"
+
+
+def run(partials, residual, gamma, eps=EPS, sm_budget=0):
+    P, R, G = to_gpu(partials, residual, gamma)
+    out = torch.empty_like(R)
+    tw.tw_fused_reduce_residual_rmsnorm(P, R, G, eps, out, sm_budget=sm_budget)
+    torch.cuda.synchronize()
+    return R, out
+
+
+def assert_same(a, b):
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ------------------------------------------------------------------ parity vs oracle
+
+SMALL = [
+    # T, H, N, p_sigma, outliers
+    (1, 8, 1, 0.05, 0.0),          # smallest row: one 16-byte vector
+    (3, 8, 16, 0.05, 0.0),         # N at its maximum
+    (7, 2056, 3, 0.02, 0.0),       # 257 vectors: a one-vector ragged chunk
+    (5, 4104, 8, 0.02, 0.0),       # 513 vectors: ragged third chunk
+    (9, 2048, 2, 0.05, 0.0),       # exactly one chunk
+    (33, 16384, 8, 0.01, 0.01),    # 405B hidden size with outliers
+    (2, 32768, 2, 0.02, 0.0),      # hidden size at its maximum (16 chunks)
+    (300, 1024, 5, 0.02, 0.0),     # more rows than SMs
+    (157, 8200, 4, 0.03, 0.0),     # ragged rows and chunks
+]
+
+
+@pytest.mark.parametrize("T,H,N,sig,outl", SMALL)
+def test_parity_small(T, H, N, sig, outl):
+    p, r, g = synth.make_inputs(T, H, N, sig, outlier_frac=outl, seed=T * 7 + N)
+    R, out = run(p, r, g)
+    check_rows(p, r, g, EPS, R, out)
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-6, 1e-5, 0.5])
+def test_parity_eps(eps):
+    p, r, g = synth.make_inputs(17, 4096, 4, 0.02, seed=5)
+    R, out = run(p, r, g, eps=eps)
+    check_rows(p, r, g, eps, R, out)
+
+
+def test_parity_pr1_workload():
+    """T=128, H=4096, N=2, P ~ N(0, 0.05^2), R ~ N(0, 1), gamma ~ N(1, 0.1^2)."""
+    p, r, g = synth.make_workload("pr1_t128_h4096_n2")
+    R, out = run(p, r, g)
+    stats = check_rows(p, r, g, EPS, R, out)
+    assert stats["rows"] == 128
+
+
+def test_parity_llama70b_all_rows():
+    """T=1024, H=8192, N=8: every row, in the launch the benchmark times."""
+    p, r, g = synth.make_workload("llama70b_t1024_h8192_n8")
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    C = math.ceil(1024 / 128) * 8
+    prefix, _ = tw.tw_wave_split(1024, C, 148)
+    s2 = torch.cuda.Stream()
+    tw.tw_run_split(prefix, P, R, G, EPS, out, torch.cuda.current_stream(), s2)
+    torch.cuda.synchronize()
+    stats = check_rows(p, r, g, EPS, R, out)
+    assert stats["max_ulp"] <= 2.0
+
+
+def test_parity_llama405b_sampled_rows():
+    """T=8192, H=16384, N=8 with 1% outliers x50: full-size launch, 256 seeded
+    random rows plus the first and last checked against the oracle."""
+    p, r, g = synth.make_workload("llama405b_t8192_h16384_n8")
+    R, out = run(p, r, g)
+    rng = np.random.Generator(np.random.PCG64(405))
+    rows = np.unique(np.concatenate([[0, 8191], rng.choice(8192, 256, replace=False)]))
+    check_rows(p, r, g, EPS, R, out, rows=rows)
+
+
+def test_zero_and_constant_rows():
+    T, H, N = 6, 4096, 3
+    p, r, g = synth.make_inputs(T, H, N, 0.02, seed=9)
+    p[:, 1] = 0
+    r[1] = 0                    # zero row -> Y = 0, not NaN
+    p[:, 2] = 0
+    r[2] = 0.75                 # constant row c -> gamma * c / sqrt(c^2 + eps)
+    R, out = run(p, r, g)
+    check_rows(p, r, g, EPS, R, out)
+    o = out.cpu().float()
+    assert torch.all(o[1] == 0)
+    want = g.float() * 0.75 / math.sqrt(0.75 ** 2 + EPS)
+    assert torch.allclose(o[2], want.to(torch.bfloat16).float(), rtol=2 ** -7, atol=0)
+
+
+def test_small_integer_partials_exact():
+    T, H, N = 4, 1024, 8
+    gen = torch.Generator().manual_seed(3)
+    p = torch.randint(-4, 5, (N, T, H), generator=gen).to(torch.bfloat16)
+    r = torch.randint(-4, 5, (T, H), generator=gen).to(torch.bfloat16)
+    g = torch.ones(H, dtype=torch.bfloat16)
+    R, out = run(p, r, g)
+    want = p.float().sum(0) + r.float()
+    assert torch.equal(R.cpu().float(), want)
+    check_rows(p, r, g, EPS, R, out)
+
+
+def test_aliased_partials_allowed():
+    T, H = 8, 4096
+    p, r, g = synth.make_inputs(T, H, 1, 0.02, seed=4)
+    P = p[0].cuda()
+    R = r.cuda()
+    G = g.cuda()
+    out = torch.empty_like(R)
+    tw.tw_fused_reduce_residual_rmsnorm([P, P, P], R, G, EPS, out)
+    torch.cuda.synchronize()
+    check_rows(torch.stack([p[0]] * 3), r, g, EPS, R, out)
+
+
+def test_inputs_not_modified():
+    p, r, g = synth.make_inputs(64, 8192, 8, 0.02, seed=6)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    tw.tw_fused_reduce_residual_rmsnorm(P, R, G, EPS, out)
+    torch.cuda.synchronize()
+    assert_same(P.cpu(), p)
+    assert_same(G.cpu(), g)
+
+
+def test_empty_batch():
+    H = 4096
+    P = torch.empty((2, 0, H), dtype=torch.bfloat16, device="cuda")
+    R = torch.empty((0, H), dtype=torch.bfloat16, device="cuda")
+    G = torch.ones(H, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(R)
+    tw.tw_fused_reduce_residual_rmsnorm(P, R, G, EPS, out)
+    torch.cuda.synchronize()
+
+
+def test_misaligned_pointer_rejected_on_device_tensors():
+    p, r, g = synth.make_inputs(4, 4096, 2, 0.02)
+    P, R, G = to_gpu(p, r, g)
+    flat = torch.empty(4 * 4096 + 8, dtype=torch.bfloat16, device="cuda")
+    out = flat[4:4 + 4 * 4096].view(4, 4096)   # 8-byte offset
+    with pytest.raises(tw.TwError) as e:
+        tw.tw_fused_reduce_residual_rmsnorm(P, R, G, EPS, out)
+    assert e.value.status == tw.TW_ERR_ALIGN
+
+
+# ------------------------------------------------------------------ bitwise invariants
+
+
+def test_repeat_runs_bitwise():
+    p, r, g = synth.make_inputs(200, 8192, 8, 0.02, seed=8)
+    a = run(p, r, g)
+    b = run(p, r, g)
+    assert_same(a[0], b[0])
+    assert_same(a[1], b[1])
+
+
+@pytest.mark.parametrize("budget", [1, 2, 3, 4, 8, 16, 151, 152, 1000])
+def test_sm_budget_bitwise(budget):
+    p, r, g = synth.make_inputs(1024, 8192, 8, 0.02, seed=1)
+    ref = run(p, r, g, sm_budget=0)
+    got = run(p, r, g, sm_budget=budget)
+    assert_same(ref[0], got[0])
+    assert_same(ref[1], got[1])
+
+
+def test_shards_bitwise_llama70b():
+    """8 token-boundary shards of 128 rows, each launched on its own, equal the
+    whole T=1024 batch bit for bit ([W] "Fix two": the norm is per token, so a
+    token-boundary shard normalises independently)."""
+    p, r, g = synth.make_workload("llama70b_t1024_h8192_n8")
+    whole_R, whole_out = run(p, r, g)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    for s in range(8):
+        a, b = s * 128, (s + 1) * 128
+        tw.tw_fused_reduce_residual_rmsnorm([P[i, a:b] for i in range(8)], R[a:b], G, EPS, out[a:b])
+    torch.cuda.synchronize()
+    assert_same(whole_R, R)
+    assert_same(whole_out, out)
+
+
+@pytest.mark.parametrize("T", [1024, 2048, 4096, 8192])
+def test_split_configs_bitwise(T):
+    """The split workload: plan with 148 SMs and C = ceil(T/128) * 8, run the
+    halves on two streams, compare with the unsplit call bit for bit."""
+    C = math.ceil(T / 128) * (8192 // 128) // 8
+    prefix, suffix = tw.tw_wave_split(T, C, 148)
+    assert (prefix, suffix) == oplanner.wave_split(T, C, 148)
+    p, r, g = synth.make_inputs(T, 8192, 8, 0.02, seed=T)
+    ref = run(p, r, g)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(sa):
+        tw.tw_run_split(prefix, P, R, G, EPS, out, sa, sb)
+    sa.synchronize()
+    assert_same(ref[0], R)
+    assert_same(ref[1], out)
+
+
+@pytest.mark.parametrize("prefix", [0, 1, 2368, 4863, 4864])
+@pytest.mark.parametrize("budget", [0, 4])
+def test_uneven_split_bitwise(prefix, budget):
+    T = 4864
+    p, r, g = synth.make_inputs(T, 8192, 8, 0.02, seed=48)
+    ref = run(p, r, g)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    tw.tw_run_split(prefix, P, R, G, EPS, out, sa, sb, sm_budget=budget)
+    sa.synchronize()
+    assert_same(ref[0], R)
+    assert_same(ref[1], out)
+
+
+def test_split_same_stream():
+    T = 300
+    p, r, g = synth.make_inputs(T, 4096, 4, 0.02, seed=30)
+    ref = run(p, r, g)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    s = torch.cuda.current_stream()
+    tw.tw_run_split(100, P, R, G, EPS, out, s, s)
+    torch.cuda.synchronize()
+    assert_same(ref[0], R)
+    assert_same(ref[1], out)
+
+
+@pytest.mark.parametrize("budget", [1, 2, 4, 8, 16])
+def test_sm_budget_occupies_at_most_budget_sms(budget):
+    T, H, N = 512, 8192, 8
+    shape = tw.tw_launch_shape(T, H, N, budget)
+    assert shape["grid"] == min(budget, T)
+    p, r, g = synth.make_inputs(T, H, N, 0.02, seed=2)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    smid = torch.full((shape["grid"],), -1, dtype=torch.int32, device="cuda")
+    tw.tw_fused_debug_smid(P, R, G, EPS, out, smid, sm_budget=budget)
+    torch.cuda.synchronize()
+    ids = smid.cpu().tolist()
+    assert min(ids) >= 0
+    assert len(set(ids)) == len(ids) <= budget   # one CTA per SM
+    check_rows(p, r, g, EPS, R, out, rows=np.arange(0, T, 37))
+
+
+def test_full_gpu_one_cta_per_sm():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shape = tw.tw_launch_shape(4096, 8192, 8, 0)
+    assert shape["grid"] == sms
+    assert shape["smem_bytes"] > 114 * 1024  # more than half an SM: one CTA per SM
+    p, r, g = synth.make_inputs(4096, 8192, 8, 0.02, seed=3)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    smid = torch.full((sms,), -1, dtype=torch.int32, device="cuda")
+    tw.tw_fused_debug_smid(P, R, G, EPS, out, smid)
+    torch.cuda.synchronize()
+    assert len(set(smid.cpu().tolist())) == sms
