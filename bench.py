@@ -203,46 +203,75 @@ def gpu_arm(args, rank, world):
     eps = 1e-5
     C = ctas_unsplit(T, H)
     bytes_step = tw.bytes_per_call(T, H, N)
-    sa = torch.cuda.current_stream(dev)
+    sa = torch.cuda.Stream(dev)  # launching stream (a created stream, so graphs can capture it)
     sb = torch.cuda.Stream(dev)
+    calls = [tw.SplitCall(s["plist"], s["R"], s["G"], eps, s["out"], sa, sb, args.sm_budget)
+             for s in sets]
+    graphs = {}
 
-    def step(k):
-        s = sets[k % len(sets)]
-        prefix, _ = tw.tw_wave_split(T, C, PLANNER_SMS)
-        tw.tw_run_split(prefix, s["plist"], s["R"], s["G"], eps, s["out"], sa, sb, args.sm_budget)
-        return prefix
+    def plan():
+        return tw.tw_wave_split(T, C, PLANNER_SMS)[0]
 
-    for k in range(args.warmup):
-        step(k)
+    def step_eager(k):
+        calls[k % len(calls)](plan())
+
+    def step_graph(k):
+        # the plan is computed every step; the graph captured for this input
+        # set and this plan is replayed (captured on first use)
+        key = (k % len(calls), plan())
+        g = graphs.get(key)
+        if g is None:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=sa):
+                calls[key[0]](key[1])
+            graphs[key] = g
+        g.replay()
+
+    step = step_graph if args.mode == "graph" else step_eager
+    sa.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(sa):
+        for k in range(max(args.warmup, len(calls))):
+            step_eager(k)
+        for k in range(args.warmup):
+            step(k)
     torch.cuda.synchronize()
     prefix, suffix = tw.tw_wave_split(T, C, PLANNER_SMS)
     launches_per_step = (1 if prefix > 0 else 0) + (1 if suffix > 0 else 0)
 
-    # per-step device durations on the launching stream (the step's kernels)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    # timed region: K steps back to back, events on the launching stream only
     clocks = ClockSampler(local) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(sa)
-    for k in range(args.steps):
-        evs[k][0].record(sa)
-        step(args.warmup + k)
-        evs[k][1].record(sa)
-    t_end.record(sa)
+    with torch.cuda.stream(sa):
+        t_start.record(sa)
+        for k in range(args.steps):
+            step(args.warmup + k)
+        t_end.record(sa)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if clocks else None
     elapsed_ms = t_start.elapsed_time(t_end)
-    step_ms = [a.elapsed_time(b) for a, b in evs]
     elapsed_ms_max = max_over_ranks(elapsed_ms, world)
     value_gbs = job_throughput(bytes_step * args.steps, elapsed_ms_max / 1e3, world) / 1e9
+    mean_step_ms = elapsed_ms / args.steps
+
+    # per-step distribution (separate pass: events between steps would
+    # serialise the programmatic launch of the next step)
+    n_dist = min(args.steps, 500)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_dist)]
+    with torch.cuda.stream(sa):
+        for k in range(n_dist):
+            evs[k][0].record(sa)
+            step(k)
+            evs[k][1].record(sa)
+    torch.cuda.synchronize()
+    step_us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
     assert tw.tw_device_status(reset=True) == 0, "a kernel gave up on a bounded wait"
 
     peak, peak_src = peak_hbm()
-    mean_step_ms = statistics.fmean(step_ms)
     achieved = bytes_step / (mean_step_ms / 1e3) / 1e9
     traffic = ncu_traffic(args.workload if not args.tokens else None)
 
@@ -258,6 +287,9 @@ def gpu_arm(args, rank, world):
             "data": "synthetic (seeded N(0,sigma^2) partials, N(0,1) residual, N(1,0.1^2) gamma)",
             "config": {"workload": args.workload, "T": T, "H": H, "N": N, "eps": eps,
                        "sm_budget": args.sm_budget, "plan": [prefix, suffix],
+                       "launch": "cuda graph per (input set, plan); plan computed every step"
+                                 if args.mode == "graph" else
+                                 "eager prepared calls, programmatic dependent launch",
                        "planner": {"ctas_unsplit": C, "num_sms": PLANNER_SMS},
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "l2": "rotating %d input sets, %.1f MB total (L2 %.1f MB): inputs larger "
@@ -270,7 +302,11 @@ def gpu_arm(args, rank, world):
                          if launches_per_step == 1 else "step (%d concurrent launches)"
                          % launches_per_step,
                          "algorithmic_bytes": bytes_step,
-                         "step_us_median": round(statistics.median(step_ms) * 1e3, 3)},
+                         "duration": "mean over the timed region's %d steps" % args.steps},
+            "step_us": {"median": round(step_us[len(step_us) // 2], 3),
+                        "p10": round(step_us[len(step_us) // 10], 3),
+                        "p90": round(step_us[(9 * len(step_us)) // 10], 3),
+                        "n": n_dist, "note": "events around each step (separate pass)"},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
@@ -281,7 +317,8 @@ def gpu_arm(args, rank, world):
 def e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb):
     """End to end through the public API with host buffers: every step copies
     the step's inputs from pinned host memory, runs the plan and the fused
-    step, and copies the updated residual and the output back."""
+    step, and copies the updated residual and the output back to pinned host
+    memory, all on the launching stream."""
     import torch
     import synth
     w = dict(synth.WORKLOADS[args.workload])
@@ -295,26 +332,27 @@ def e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb):
     R = torch.empty_like(r, device=dev)
     G = torch.empty_like(g, device=dev)
     out = torch.empty_like(R)
-    plist = [P[i] for i in range(N)]
+    call = tw.SplitCall([P[i] for i in range(N)], R, G, eps, out, sa, sb, args.sm_budget)
     steps = max(3, min(args.e2e_steps, args.steps))
 
     def step():
         P.copy_(hp, non_blocking=True)
         R.copy_(hr, non_blocking=True)
         G.copy_(hg, non_blocking=True)
-        prefix, _ = tw.tw_wave_split(T, C, PLANNER_SMS)
-        tw.tw_run_split(prefix, plist, R, G, eps, out, sa, sb, args.sm_budget)
+        call(tw.tw_wave_split(T, C, PLANNER_SMS)[0])
         hr_out.copy_(R, non_blocking=True)
         hy_out.copy_(out, non_blocking=True)
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(sa)
-    for _ in range(steps):
-        step()
-    b.record(sa)
+    sa.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(sa):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(sa)
+        for _ in range(steps):
+            step()
+        b.record(sa)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     h2d = (N + 1) * T * H * 2 + H * 2
@@ -455,6 +493,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama70b_t1024_h8192_n8")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's T")
     ap.add_argument("--sm-budget", type=int, default=0)
+    ap.add_argument("--mode", choices=("eager", "graph"), default="eager")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")

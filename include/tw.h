@@ -149,9 +149,13 @@ int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_sms, const t
  * (so up to 2 * sm_budget SMs while both run). stream_b first waits for the
  * work already queued on stream_a; on return stream_a is ordered after both
  * halves. An empty half is not launched. The result is bitwise the same as
- * the unsplit call. The call creates two CUDA events and destroys them before
- * returning; it never destroys the streams. stream_a == stream_b is allowed
- * (the halves then run in order).
+ * the unsplit call. The fork and join use two CUDA events per device that
+ * each calling host thread creates on first use and keeps; the call never
+ * creates or destroys streams. stream_a == stream_b is allowed (the halves
+ * then run in order, with no events). The call can be captured into a CUDA
+ * graph (the two streams become a fork and a join in the graph) once an
+ * eager call of the same shape has run on the thread, so that the kernel's
+ * attributes and the events already exist.
  *
  * Arguments as for the fused call, plus prefix_tokens in [0, T].
  */

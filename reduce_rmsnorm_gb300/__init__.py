@@ -14,6 +14,9 @@ The functions carry the C names:
     tw_launch_shape(T, H, N, sm_budget=0)
     tw_device_status(reset=True)
     tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=None, sm_budget=0)
+
+For launch-bound loops, ``FusedCall`` and ``SplitCall`` marshal the arguments
+once and then launch with a single ctypes call each time they are called.
 """
 
 import ctypes
@@ -182,6 +185,46 @@ def tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a=No
     st = lib().tw_run_split(int(prefix_tokens), arr, n, _ptr(residual), _ptr(gamma), float(eps), T,
                             H, _ptr(out), _stream(stream_a), _stream(stream_b), int(sm_budget))
     _check(st, "tw_run_split")
+
+
+class FusedCall:
+    """tw_fused_reduce_residual_rmsnorm with its arguments marshalled once.
+
+    Holds references to the tensors; calling the object launches the step on
+    the stream resolved at construction."""
+
+    def __init__(self, partials, residual, gamma, eps, out, stream=None, sm_budget=0):
+        arr, n = _partials_array(partials)
+        T, H = _shape(residual)
+        self.tensors = (partials, residual, gamma, out)
+        self._fn = lib().tw_fused_reduce_residual_rmsnorm
+        self._args = (arr, n, _ptr(residual), _ptr(gamma), ctypes.c_float(eps), T, H, _ptr(out),
+                      _stream(stream), int(sm_budget))
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != TW_OK:
+            raise TwError(st, "tw_fused_reduce_residual_rmsnorm")
+
+
+class SplitCall:
+    """tw_run_split with its arguments marshalled once; call it with the
+    prefix token count."""
+
+    def __init__(self, partials, residual, gamma, eps, out, stream_a=None, stream_b=None,
+                 sm_budget=0):
+        arr, n = _partials_array(partials)
+        T, H = _shape(residual)
+        self.tokens = T
+        self.tensors = (partials, residual, gamma, out)
+        self._fn = lib().tw_run_split
+        self._args = (arr, n, _ptr(residual), _ptr(gamma), ctypes.c_float(eps), T, H, _ptr(out),
+                      _stream(stream_a), _stream(stream_b), int(sm_budget))
+
+    def __call__(self, prefix_tokens):
+        st = self._fn(int(prefix_tokens), *self._args)
+        if st != TW_OK:
+            raise TwError(st, "tw_run_split")
 
 
 def tw_launch_shape(T, H, N, sm_budget=0):

@@ -61,6 +61,30 @@ int validate(const void* const* partials, int N, void* residual, const void* gam
   return TW_OK;
 }
 
+// Two events per device for the split's fork and join, created on first use
+// by each host thread and kept for the thread's lifetime (an event is reused
+// only after the stream-wait that consumed its previous record was enqueued).
+constexpr int kMaxDevices = 64;
+struct SplitEvents {
+  cudaEvent_t fork[kMaxDevices] = {};
+  cudaEvent_t join[kMaxDevices] = {};
+};
+thread_local SplitEvents t_events;
+
+int split_events(cudaEvent_t* fork, cudaEvent_t* join) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TW_ERR_CUDA;
+  if (!t_events.fork[dev] &&
+      cudaEventCreateWithFlags(&t_events.fork[dev], cudaEventDisableTiming) != cudaSuccess)
+    return TW_ERR_CUDA;
+  if (!t_events.join[dev] &&
+      cudaEventCreateWithFlags(&t_events.join[dev], cudaEventDisableTiming) != cudaSuccess)
+    return TW_ERR_CUDA;
+  *fork = t_events.fork[dev];
+  *join = t_events.join[dev];
+  return TW_OK;
+}
+
 // Rows [row0, row0 + rows) of a validated call.
 tw::FusedArgs slice(const tw::FusedArgs& a, int64_t row0, int64_t rows) {
   tw::FusedArgs s = a;
@@ -122,23 +146,17 @@ extern "C" int tw_run_split(int64_t prefix_tokens, const void* const* partials, 
       return TW_OK;
     }
     cudaEvent_t fork = nullptr, join = nullptr;
-    if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return TW_ERR_CUDA;
-    if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
-      cudaEventDestroy(fork);
-      return TW_ERR_CUDA;
-    }
-    st = TW_OK;
+    if ((st = split_events(&fork, &join)) != TW_OK) return st;
     if (cudaEventRecord(fork, sa) != cudaSuccess || cudaStreamWaitEvent(sb, fork, 0) != cudaSuccess)
-      st = TW_ERR_CUDA;
-    if (st == TW_OK && prefix_tokens > 0)
-      st = tw::launch_fused(slice(a, 0, prefix_tokens), sa, sm_budget, nullptr);
-    if (st == TW_OK) st = tw::launch_fused(slice(a, prefix_tokens, suffix), sb, sm_budget, nullptr);
-    if (st == TW_OK &&
-        (cudaEventRecord(join, sb) != cudaSuccess || cudaStreamWaitEvent(sa, join, 0) != cudaSuccess))
-      st = TW_ERR_CUDA;
-    cudaEventDestroy(fork);
-    cudaEventDestroy(join);
-    return st;
+      return TW_ERR_CUDA;
+    if (prefix_tokens > 0 &&
+        (st = tw::launch_fused(slice(a, 0, prefix_tokens), sa, sm_budget, nullptr)) != TW_OK)
+      return st;
+    if ((st = tw::launch_fused(slice(a, prefix_tokens, suffix), sb, sm_budget, nullptr)) != TW_OK)
+      return st;
+    if (cudaEventRecord(join, sb) != cudaSuccess || cudaStreamWaitEvent(sa, join, 0) != cudaSuccess)
+      return TW_ERR_CUDA;
+    return TW_OK;
   } catch (...) {
     return TW_ERR_CUDA;
   }

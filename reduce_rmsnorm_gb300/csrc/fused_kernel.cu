@@ -12,21 +12,28 @@
 //     second CTA of this kernel fits), each owning a contiguous range of token
 //     rows ([W]'s tokens_per_cta = ceil(num_tokens / gridDim.x), balanced).
 //     The grid size is the SM budget.
-//   * Warp-specialised: one producer lane streams each row, in 4 KiB chunks of
-//     every source (N partials + residual), from HBM into a ring of shared
-//     memory stages with 1-D TMA bulk copies (cp.async.bulk, mbarrier
-//     completion, L2 evict-first). Eight consumer warps read a chunk (one
-//     16-byte vector per thread per source), sum in fp32 in rank order, add
-//     the residual, store the updated residual, and keep z in registers.
+//   * Warp-specialised: the producer warp streams each row, in chunks of 8 KiB
+//     (N <= 8) or 4 KiB of every source (N partials + residual), from HBM into
+//     a ring of shared-memory stages with 1-D TMA bulk copies (cp.async.bulk,
+//     mbarrier completion, L2 evict-first); lane r issues source r's copy, so
+//     the N + 1 copies of a stage go out in parallel (one lane issuing them in
+//     turn, or 4 KiB copies, caps an SM near 45 GB/s). Eight consumer warps
+//     read a chunk (one or two 16-byte vectors per thread per source), sum in
+//     fp32 in rank order, add the residual, store the updated residual, and
+//     keep z in registers.
 //   * After a row's last chunk: warp xor-shuffle sum of squares, a fixed-order
 //     combine of the 8 warp sums, rsqrtf, and Y = (z * r) * gamma stored with
 //     16-byte stores. The per-row arithmetic depends only on H, so every grid
 //     size (SM budget), split and shard gives bitwise the same rows.
+//   * Programmatic dependent launch: the CTAs set up their barriers while the
+//     previous kernel in the stream drains, then wait (griddepcontrol.wait)
+//     before touching global memory.
 //   * Every wait on an mbarrier is bounded (time and iterations); on giving up
 //     the CTA sets a device error word and finishes without further waits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -43,8 +50,10 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kChunkVec = kConsumerThreads;      // 16-byte vectors per source per chunk
-constexpr int kChunkBytes = kChunkVec * 16;      // 4 KiB
+// A "slot" is one 16-byte vector per consumer thread: 256 vectors, 4 KiB of a
+// source row. A chunk (the unit of one bulk copy per source) is VPT slots.
+constexpr int kSlotVec = kConsumerThreads;
+constexpr int kSlotBytes = kSlotVec * 16;
 constexpr int kMaxStages = 32;
 constexpr int kConsumerBarrierId = 1;            // named barrier of the consumer warps
 
@@ -61,7 +70,7 @@ struct Params {
   long long rows;
   int vec_per_row;  // H / 8
   int n_partials;
-  int chunks;       // ceil(vec_per_row / kChunkVec)
+  int chunks;       // ceil(vec_per_row / (kSlotVec * VPT))
   int stages;
   float eps;
   float hidden;
@@ -138,6 +147,14 @@ __device__ __forceinline__ void consumer_barrier() {
   asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrierId), "n"(kConsumerThreads) : "memory");
 }
 
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t sm_id() {
   uint32_t id;
   asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
@@ -204,7 +221,41 @@ __device__ __forceinline__ uint4 pack8(const float a[8]) {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int KMAX>
+// Sum of the N partials and the residual for one 16-byte vector column of a
+// staged chunk, in rank order, residual last. `src` addresses the column in
+// source 0's chunk; source r's chunk is `cbytes` further per r. NT > 0: N is a
+// compile-time constant and all N + 1 shared loads issue before the first
+// add; NT == 0: runtime N.
+template <int NT>
+__device__ __forceinline__ void reduce_vector(uint32_t src, uint32_t cbytes, int n, float a[8]) {
+  if constexpr (NT > 0) {
+    uint4 q[NT + 1];
+#pragma unroll
+    for (int r = 0; r <= NT; ++r) q[r] = lds128(src + r * cbytes);
+    load8(q[0], a);
+#pragma unroll
+    for (int r = 1; r <= NT; ++r) add8(q[r], a);
+  } else {
+    load8(lds128(src), a);
+    int r = 1;
+    for (; r + 3 < n; r += 4) {
+      const uint4 q0 = lds128(src + r * cbytes), q1 = lds128(src + (r + 1) * cbytes);
+      const uint4 q2 = lds128(src + (r + 2) * cbytes), q3 = lds128(src + (r + 3) * cbytes);
+      add8(q0, a); add8(q1, a); add8(q2, a); add8(q3, a);
+    }
+    for (; r < n; ++r) add8(lds128(src + r * cbytes), a);
+    add8(lds128(src + n * cbytes), a);  // residual last
+  }
+}
+
+// KMAX: slots of a row held in registers (ceil(H/8 / 256) rounded up to a
+//       power of two, >= VPT).
+// VPT:  slots per chunk (1: 4 KiB copies; 2: 8 KiB copies).
+// NT:   compile-time partial count, or 0 for any N.
+// Thread t of the consumers owns vectors t, t + 256, t + 512, ... of every row
+// (slot j = vector j * 256 + t) whatever VPT is, so the per-row arithmetic,
+// including the order of the sum of squares, depends only on H.
+template <int KMAX, int VPT, int NT>
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -212,13 +263,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   __shared__ float warp_ss[2][kConsumerWarps];
   __shared__ int abort_flag;
 
+  constexpr int kChunkVec = kSlotVec * VPT;
+  constexpr uint32_t kChunkBytes = kSlotBytes * VPT;
+  static_assert(KMAX % VPT == 0, "slots must fill whole chunks");
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const long long grid = gridDim.x;
   const long long row0 = static_cast<long long>(blockIdx.x) * p.rows / grid;
   const long long row1 = static_cast<long long>(blockIdx.x + 1) * p.rows / grid;
-  const int n = p.n_partials;
+  const int n = NT > 0 ? NT : p.n_partials;
   const int vpr = p.vec_per_row;
   const int chunks = p.chunks;
   const int stages = p.stages;
@@ -231,15 +285,24 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     }
     abort_flag = 0;
     fence_mbar_init();
-    if (p.smid_out) p.smid_out[blockIdx.x] = static_cast<int>(sm_id());
   }
   __syncthreads();
+  // Programmatic dependent launch: this CTA may be resident before the
+  // previous kernel in the stream has finished. Nothing above touched global
+  // memory; wait here until that kernel has completed and its writes are
+  // visible, then allow the next kernel in the stream to start launching.
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (tid == 0 && p.smid_out) p.smid_out[blockIdx.x] = static_cast<int>(sm_id());
   volatile int* abort = &abort_flag;
 
   if (warp == kConsumerWarps) {
-    // ---------------- producer: one lane streams (row, chunk) items into the ring
-    if (lane != 0) return;
+    // ---------------- producer: lanes 0..N stream (row, chunk) items into the
+    // ring; lane r < N copies partial r, lane N the residual.
+    if (lane > n) return;
+    const unsigned lanes = n + 1 == 32 ? 0xffffffffu : ((1u << (n + 1)) - 1u);
     const uint64_t policy = l2_evict_first_policy();
+    const uint4* src_base = lane < n ? p.partials[lane] : p.residual;
     const long long items = (row1 - row0) * chunks;
     long long issued = 0;
     long long row = row0;
@@ -247,21 +310,22 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     uint32_t round_parity = 0;  // parity of the current pass over the ring
     bool first_pass = true;
     for (long long it = 0; it < items; ++it) {
-      if (!first_pass && !wait_phase(&empty_bar[s], round_parity ^ 1u, abort, 2u)) break;
+      int ok = 1;
       const int v0 = chunk * kChunkVec;
       const int nvec = min(kChunkVec, vpr - v0);
       const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
-      mbar_arrive_expect_tx(&full_bar[s], bytes * static_cast<uint32_t>(n + 1));
-      unsigned char* dst = ring + static_cast<size_t>(s) * stage_bytes;
-      const long long off = row * vpr + v0;
-      for (int r = 0; r < n; ++r)
-        bulk_load(dst + r * kChunkBytes, p.partials[r] + off, bytes, &full_bar[s], policy);
-      bulk_load(dst + n * kChunkBytes, p.residual + off, bytes, &full_bar[s], policy);
+      if (lane == 0) {
+        if (!first_pass) ok = wait_phase(&empty_bar[s], round_parity ^ 1u, abort, 2u);
+        if (ok) mbar_arrive_expect_tx(&full_bar[s], bytes * static_cast<uint32_t>(n + 1));
+      }
+      if (!__shfl_sync(lanes, ok, 0)) break;
+      bulk_load(ring + static_cast<size_t>(s) * stage_bytes + lane * kChunkBytes,
+                src_base + row * vpr + v0, bytes, &full_bar[s], policy);
       ++issued;
       if (++chunk == chunks) { chunk = 0; ++row; }
       if (++s == stages) { s = 0; round_parity ^= 1u; first_pass = false; }
     }
-    if (*abort) {
+    if (lane == 0 && *abort) {
       // Let every copy this CTA issued land before the CTA exits: the last
       // item issued on each stage completes after all earlier ones there.
       const long long last = issued - 1;
@@ -273,9 +337,19 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     return;
   }
 
-  // ---------------- consumers: 8 warps, thread t owns vectors t, t+256, ... of each row
+  // ---------------- consumers: 8 warps; thread t owns slots j (vector j*256 + t)
   const int t = tid;
   const uint32_t ring_base = smem_addr(ring) + static_cast<uint32_t>(t) * 16u;
+  // gamma stays in registers for the CTA's whole row range (read once per CTA)
+  constexpr bool kGammaRegs = KMAX <= 8;
+  uint4 g_reg[kGammaRegs ? KMAX : 1];
+  if constexpr (kGammaRegs) {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const int v = j * kSlotVec + t;
+      g_reg[j] = v < vpr ? __ldg(p.gamma + v) : make_uint4(0, 0, 0, 0);
+    }
+  }
   int s = 0;
   uint32_t parity = 0;
   float z[KMAX][8];
@@ -283,27 +357,26 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     float ss = 0.0f;
     uint4* res_row = p.residual + row * vpr;
 #pragma unroll
-    for (int k = 0; k < KMAX; ++k) {
-      if (k < chunks) {
-        const int v = k * kChunkVec + t;
-        const bool active = v < vpr;
+    for (int c = 0; c < KMAX / VPT; ++c) {
+      if (c < chunks) {
         wait_phase(&full_bar[s], parity, abort, 1u);
-        float a[8];
-        if (active) {
-          const uint32_t src = ring_base + static_cast<uint32_t>(s) * stage_bytes;
-          load8(lds128(src), a);
-          for (int r = 1; r < n; ++r) add8(lds128(src + r * kChunkBytes), a);
-          add8(lds128(src + n * kChunkBytes), a);  // residual last
+        const uint32_t stage = ring_base + static_cast<uint32_t>(s) * stage_bytes;
+#pragma unroll
+        for (int u = 0; u < VPT; ++u) {
+          const int j = c * VPT + u;
+          if (j * kSlotVec + t < vpr) reduce_vector<NT>(stage + u * kSlotBytes, kChunkBytes, n, z[j]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
-        if (active) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            z[k][i] = a[i];
-            ss = fmaf(a[i], a[i], ss);
+        for (int u = 0; u < VPT; ++u) {
+          const int j = c * VPT + u;
+          const int v = j * kSlotVec + t;
+          if (v < vpr) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss = fmaf(z[j][i], z[j][i], ss);
+            res_row[v] = pack8(z[j]);
           }
-          res_row[v] = pack8(a);
         }
         if (++s == stages) { s = 0; parity ^= 1u; }
       }
@@ -319,13 +392,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     const float rs = rsqrtf(total / p.hidden + p.eps);
     uint4* out_row = p.out + row * vpr;
 #pragma unroll
-    for (int k = 0; k < KMAX; ++k) {
-      const int v = k * kChunkVec + t;
-      if (k < chunks && v < vpr) {
+    for (int j = 0; j < KMAX; ++j) {
+      const int v = j * kSlotVec + t;
+      if (v < vpr) {
         float g[8], y[8];
-        load8(__ldg(p.gamma + v), g);
+        if constexpr (kGammaRegs) load8(g_reg[j], g);
+        else load8(__ldg(p.gamma + v), g);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = (z[k][i] * rs) * g[i];
+        for (int i = 0; i < 8; ++i) y[i] = (z[j][i] * rs) * g[i];
         out_row[v] = pack8(y);
       }
     }
@@ -337,43 +411,89 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
 constexpr int kMaxDevices = 64;
 constexpr int kStaticSmemReserve = 2048;  // barriers, warp sums, flag, slack
 
+using KernelFn = void (*)(Params);
+
+// Kernel instances. VPT = 2 (8 KiB copies) serves N <= 8 with a compile-time
+// N for 2, 4 and 8; VPT = 1 (4 KiB copies) serves N = 9..16, whose stages
+// would not fit three deep at 8 KiB.
+#define TW_NROW(K) {fused_kernel<K, 2, 0>, fused_kernel<K, 2, 2>, fused_kernel<K, 2, 4>, \
+                    fused_kernel<K, 2, 8>}
+const KernelFn kVpt2[4][4] = {TW_NROW(2), TW_NROW(4), TW_NROW(8), TW_NROW(16)};
+#undef TW_NROW
+const KernelFn kVpt1[5] = {fused_kernel<1, 1, 0>, fused_kernel<2, 1, 0>, fused_kernel<4, 1, 0>,
+                           fused_kernel<8, 1, 0>, fused_kernel<16, 1, 0>};
+constexpr int kNumKernels = 16 + 5;
+
+// Per-device attributes, queried once; the launch path reads them without a
+// lock once `ready` is set (the flags live in static storage, so they start
+// false).
 struct DeviceInfo {
-  bool ready = false;
-  int sms = 0;
-  int smem_optin = 0;
-  bool attr_done[5] = {false, false, false, false, false};
+  std::atomic<bool> ready;
+  int sms;
+  int smem_optin;
+  std::atomic<bool> attr_done[kNumKernels];
 };
 
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_mutex;
 
-int kmax_index(int chunks) {
-  if (chunks <= 1) return 0;
-  if (chunks <= 2) return 1;
-  if (chunks <= 4) return 2;
-  if (chunks <= 8) return 3;
-  return 4;
+int log2_pow2_at_least(int x) {
+  int k = 0;
+  while ((1 << k) < x) ++k;
+  return k;
 }
 
-using KernelFn = void (*)(Params);
-const KernelFn kKernels[5] = {fused_kernel<1>, fused_kernel<2>, fused_kernel<4>, fused_kernel<8>,
-                              fused_kernel<16>};
+int partials_index(int n) { return n == 2 ? 1 : n == 4 ? 2 : n == 8 ? 3 : 0; }
 
-int device_info(DeviceInfo** out, int* dev_out) {
+int vpt_for(int n) { return n <= 8 ? 2 : 1; }
+
+// Which instance serves (H/8 vectors, N): its table index and kernel.
+void select_kernel(int vpr, int n, int* index, KernelFn* fn, int* kmax) {
+  const int vpt = vpt_for(n);
+  const int chunks = (vpr + kSlotVec * vpt - 1) / (kSlotVec * vpt);
+  const int k = log2_pow2_at_least(chunks * vpt);  // KMAX = 2^k
+  *kmax = 1 << k;
+  if (vpt == 2) {
+    const int ki = k - 1, ni = partials_index(n);  // KMAX 2..16
+    *index = ki * 4 + ni;
+    *fn = kVpt2[ki][ni];
+  } else {
+    *index = 16 + k;  // KMAX 1..16
+    *fn = kVpt1[k];
+  }
+}
+
+int device_info(DeviceInfo** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TW_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mutex);
   DeviceInfo& d = g_devices[dev];
-  if (!d.ready) {
-    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return TW_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-        cudaSuccess)
-      return TW_ERR_CUDA;
-    d.ready = true;
+  if (!d.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!d.ready.load(std::memory_order_relaxed)) {
+      if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return TW_ERR_CUDA;
+      if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+          cudaSuccess)
+        return TW_ERR_CUDA;
+      d.ready.store(true, std::memory_order_release);
+    }
   }
   *out = &d;
-  *dev_out = dev;
+  return TW_OK;
+}
+
+int shape_for(const DeviceInfo& d, int64_t rows, int n, int sm_budget, LaunchShape* shape) {
+  const int stage_bytes = (n + 1) * kSlotBytes * vpt_for(n);
+  int stages = (d.smem_optin - kStaticSmemReserve) / stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return TW_ERR_UNSUPPORTED;
+  int grid = d.sms;
+  if (sm_budget > 0 && sm_budget < grid) grid = sm_budget;
+  if (rows < grid) grid = static_cast<int>(rows);
+  shape->grid = grid;
+  shape->threads = kThreads;
+  shape->smem_bytes = stages * stage_bytes;
+  shape->stages = stages;
   return TW_OK;
 }
 
@@ -381,29 +501,22 @@ int device_info(DeviceInfo** out, int* dev_out) {
 
 int plan_launch(int64_t rows, int64_t hidden, int n, int sm_budget, LaunchShape* shape) {
   DeviceInfo* d = nullptr;
-  int dev = 0;
-  const int st = device_info(&d, &dev);
+  int st = device_info(&d);
   if (st != TW_OK) return st;
-  const int vpr = static_cast<int>(hidden / 8);
-  const int chunks = (vpr + kChunkVec - 1) / kChunkVec;
-  const int stage_bytes = (n + 1) * kChunkBytes;
-  int stages = (d->smem_optin - kStaticSmemReserve) / stage_bytes;
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2) return TW_ERR_UNSUPPORTED;
-  int grid = d->sms;
-  if (sm_budget > 0 && sm_budget < grid) grid = sm_budget;
-  if (rows < grid) grid = static_cast<int>(rows);
-  shape->grid = grid;
-  shape->threads = kThreads;
-  shape->smem_bytes = stages * stage_bytes;
-  shape->stages = stages;
-  shape->kmax = 1 << kmax_index(chunks);
+  st = shape_for(*d, rows, n, sm_budget, shape);
+  if (st != TW_OK) return st;
+  int index = 0;
+  KernelFn fn = nullptr;
+  select_kernel(static_cast<int>(hidden / 8), n, &index, &fn, &shape->kmax);
   return TW_OK;
 }
 
 int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* smid_out) {
+  DeviceInfo* d = nullptr;
+  int st = device_info(&d);
+  if (st != TW_OK) return st;
   LaunchShape shape;
-  int st = plan_launch(a.rows, a.hidden, a.n, sm_budget, &shape);
+  st = shape_for(*d, a.rows, a.n, sm_budget, &shape);
   if (st != TW_OK) return st;
   if (shape.grid <= 0) return TW_OK;
 
@@ -417,28 +530,43 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
   p.rows = a.rows;
   p.vec_per_row = static_cast<int>(a.hidden / 8);
   p.n_partials = a.n;
-  p.chunks = (p.vec_per_row + kChunkVec - 1) / kChunkVec;
+  const int chunk_vec = kSlotVec * vpt_for(a.n);
+  p.chunks = (p.vec_per_row + chunk_vec - 1) / chunk_vec;
   p.stages = shape.stages;
   p.eps = a.eps;
   p.hidden = static_cast<float>(a.hidden);
 
-  const int ki = kmax_index(p.chunks);
-  DeviceInfo* d = nullptr;
-  int dev = 0;
-  st = device_info(&d, &dev);
-  if (st != TW_OK) return st;
-  {
+  int index = 0, kmax = 0;
+  KernelFn fn = nullptr;
+  select_kernel(p.vec_per_row, a.n, &index, &fn, &kmax);
+  if (!d->attr_done[index].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!d->attr_done[ki]) {
+    if (!d->attr_done[index].load(std::memory_order_relaxed)) {
       const int max_dyn = d->smem_optin - kStaticSmemReserve;
-      if (cudaFuncSetAttribute(kKernels[ki], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               max_dyn) != cudaSuccess)
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn) !=
+          cudaSuccess)
         return TW_ERR_CUDA;
-      d->attr_done[ki] = true;
+      d->attr_done[index].store(true, std::memory_order_release);
     }
   }
-  kKernels[ki]<<<shape.grid, kThreads, shape.smem_bytes, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? TW_OK : TW_ERR_CUDA;
+  // Launched with programmatic stream serialization: the CTAs may start while
+  // the previous kernel in the stream drains (the kernel waits on
+  // griddepcontrol.wait before any global-memory access).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(shape.grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(shape.smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) {
+    cudaGetLastError();
+    return TW_ERR_CUDA;
+  }
+  return TW_OK;
 }
 
 int read_device_error(int reset, int* code) {
