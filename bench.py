@@ -269,6 +269,29 @@ def gpu_arm(args, rank, world):
             evs[k][1].record(sa)
     torch.cuda.synchronize()
     step_us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+
+    # the unfused baseline (reduce -> HBM -> residual add + RMSNorm) on the same
+    # rotating sets, timed the same way, for the fusion ratio
+    unfused = None
+    if not args.no_unfused:
+        ucalls = [tw.UnfusedCall(s["plist"], s["R"], s["G"], eps, s["out"], sa) for s in sets]
+        n_u = min(args.steps, 2000)
+        with torch.cuda.stream(sa):
+            for k in range(max(args.warmup, len(ucalls))):
+                ucalls[k % len(ucalls)]()
+            u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            u0.record(sa)
+            for k in range(n_u):
+                ucalls[k % len(ucalls)]()
+            u1.record(sa)
+        torch.cuda.synchronize()
+        u_ms = u0.elapsed_time(u1) / n_u
+        u_bytes = (N + 5) * T * H * 2 + H * 2
+        unfused = {"us_per_step": round(u_ms * 1e3, 3), "steps": n_u, "launches_per_step": 2,
+                   "hbm_bytes_per_step": u_bytes,
+                   "GB_s_on_fused_bytes": round(bytes_step / (u_ms / 1e3) / 1e9, 2),
+                   "GB_s_on_own_bytes": round(u_bytes / (u_ms / 1e3) / 1e9, 2),
+                   "fused_speedup": round(u_ms / mean_step_ms, 4)}
     assert tw.tw_device_status(reset=True) == 0, "a kernel gave up on a bounded wait"
 
     peak, peak_src = peak_hbm()
@@ -307,7 +330,7 @@ def gpu_arm(args, rank, world):
                         "p10": round(step_us[len(step_us) // 10], 3),
                         "p90": round(step_us[(9 * len(step_us)) // 10], 3),
                         "n": n_dist, "note": "events around each step (separate pass)"},
-            "cpu_baseline": cpu, "e2e": e2e,
+            "unfused": unfused, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
@@ -468,13 +491,28 @@ def sweep(args):
             med = us[len(us) // 2]
             used = tw.tw_launch_shape(T, H, N, budget)["grid"]
             gbs = bytes_call / (med / 1e6) / 1e9
+            extra = {}
+            if budget == 0:
+                ucalls = [tw.UnfusedCall(s["plist"], s["R"], s["G"], 1e-5, s["out"]) for s in sets]
+                for k in range(3):
+                    ucalls[k % len(ucalls)]()
+                torch.cuda.synchronize()
+                uevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                        for _ in range(reps)]
+                for k in range(reps):
+                    uevs[k][0].record()
+                    ucalls[k % len(ucalls)]()
+                    uevs[k][1].record()
+                torch.cuda.synchronize()
+                uus = sorted(a.elapsed_time(b) * 1e3 for a, b in uevs)[reps // 2]
+                extra = {"unfused_us_median": round(uus, 2), "fused_speedup": round(uus / med, 3)}
             print(json.dumps({"T": T, "H": H, "N": N, "sm_budget": budget or "full",
                               "sms_used": used, "us_median": round(med, 2),
                               "us_p10": round(us[len(us) // 10], 2),
                               "us_p90": round(us[(9 * len(us)) // 10], 2),
                               "GB_s": round(gbs, 1), "GB_s_per_sm": round(gbs / used, 2),
                               "hbm_frac": round(gbs / peak, 4),
-                              "tokens_per_s": round(T / (med / 1e6), 1), "sms": sms}),
+                              "tokens_per_s": round(T / (med / 1e6), 1), "sms": sms, **extra}),
                   flush=True)
         del sets
         torch.cuda.empty_cache()
@@ -496,6 +534,7 @@ def main(argv=None):
     ap.add_argument("--mode", choices=("eager", "graph"), default="eager")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-tokens", default="512,1024,2048,4096,8192,16384")
     ap.add_argument("--sweep-budgets", default="2,4,8,16,0")

@@ -195,6 +195,38 @@ int tw_fused_debug_smid(const void* const* partials, int N, void* residual, cons
                         float eps, int64_t T, int64_t H, void* out, tw_stream_t stream,
                         int sm_budget, int* smid_out);
 
+/*
+ * Unfused baseline: the two kernels the fused step replaces, for measuring
+ * what the fusion saves on one GPU ([W] "Fix two": vLLM normalises after the
+ * all-reduce has written its result; [G] "The Standard RMSNorm Memory
+ * Round-Trip": the reduced tensor goes to HBM and a separate kernel reads it
+ * back). Together they compute the same step with two extra bf16 roundings
+ * and (N+5)*T*H*2 bytes of HBM traffic instead of (N+3)*T*H*2.
+ *
+ * tw_reduce_partials: sum_out[t] = bf16_rne(((P_0[t] + P_1[t]) + ...) + P_{N-1}[t]),
+ * fp32 adds in rank order.
+ *   partials   host array of N device pointers, bf16 [T, H], read only.
+ *   sum_out    device bf16 [T, H], written; must not overlap a partial.
+ *   Other arguments and errors as for the fused call (N 1..16, H % 8 == 0,
+ *   16-byte aligned pointers, T == 0 a no-op).
+ */
+int tw_reduce_partials(const void* const* partials, int N, int64_t T, int64_t H, void* sum_out,
+                       tw_stream_t stream);
+
+/*
+ * tw_add_rmsnorm: a standalone residual add + RMSNorm over the stored sum:
+ *     x = fp32(sum[t]) + fp32(residual[t]);  residual[t] = bf16_rne(x);
+ *     r = rsqrt(sum_j residual[t]_j^2 / H + eps)   (on the stored bf16 values)
+ *     out[t] = bf16_rne((residual[t] * r) * gamma)
+ *   sum        device bf16 [T, H], read only; may be the same pointer as out
+ *              (each row is read before it is written), otherwise must not
+ *              overlap out.
+ *   residual   device bf16 [T, H], in/out; must not overlap sum, out or gamma.
+ *   Other arguments and errors as for the fused call.
+ */
+int tw_add_rmsnorm(const void* sum, void* residual, const void* gamma, float eps, int64_t T,
+                   int64_t H, void* out, tw_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

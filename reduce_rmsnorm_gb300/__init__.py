@@ -14,6 +14,8 @@ The functions carry the C names:
     tw_launch_shape(T, H, N, sm_budget=0)
     tw_device_status(reset=True)
     tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=None, sm_budget=0)
+    tw_reduce_partials(partials, sum_out, stream=None)                 # unfused baseline
+    tw_add_rmsnorm(sum_in, residual, gamma, eps, out, stream=None)     # unfused baseline
 
 For launch-bound loops, ``FusedCall`` and ``SplitCall`` marshal the arguments
 once and then launch with a single ctypes call each time they are called.
@@ -38,7 +40,8 @@ DEFAULT_OFFSETS = (0, 64, 128, 192, 256, 512)
 DEFAULT_MIN_SPLIT_TOKENS = 1024
 
 EXPORTED = ("tw_fused_reduce_residual_rmsnorm", "tw_wave_split", "tw_run_split", "tw_strerror",
-            "tw_launch_shape", "tw_device_status", "tw_fused_debug_smid")
+            "tw_launch_shape", "tw_device_status", "tw_fused_debug_smid", "tw_reduce_partials",
+            "tw_add_rmsnorm")
 
 
 class TwError(RuntimeError):
@@ -87,6 +90,10 @@ def lib():
     L.tw_launch_shape.restype = _int
     L.tw_device_status.argtypes = [_int, ctypes.POINTER(_int)]
     L.tw_device_status.restype = _int
+    L.tw_reduce_partials.argtypes = [ctypes.POINTER(_vp), _int, _i64, _i64, _vp, _vp]
+    L.tw_reduce_partials.restype = _int
+    L.tw_add_rmsnorm.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp]
+    L.tw_add_rmsnorm.restype = _int
     _lib = L
     return L
 
@@ -187,6 +194,22 @@ def tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a=No
     _check(st, "tw_run_split")
 
 
+def tw_reduce_partials(partials, sum_out, stream=None):
+    """Unfused baseline, kernel 1: sum_out <- bf16(sum of the partials)."""
+    arr, n = _partials_array(partials)
+    T, H = _shape(sum_out)
+    st = lib().tw_reduce_partials(arr, n, T, H, _ptr(sum_out), _stream(stream))
+    _check(st, "tw_reduce_partials")
+
+
+def tw_add_rmsnorm(sum_in, residual, gamma, eps, out, stream=None):
+    """Unfused baseline, kernel 2: residual <- bf16(sum + residual); out <- RMSNorm(residual)."""
+    T, H = _shape(residual)
+    st = lib().tw_add_rmsnorm(_ptr(sum_in), _ptr(residual), _ptr(gamma), float(eps), T, H,
+                              _ptr(out), _stream(stream))
+    _check(st, "tw_add_rmsnorm")
+
+
 class FusedCall:
     """tw_fused_reduce_residual_rmsnorm with its arguments marshalled once.
 
@@ -225,6 +248,28 @@ class SplitCall:
         st = self._fn(int(prefix_tokens), *self._args)
         if st != TW_OK:
             raise TwError(st, "tw_run_split")
+
+
+class UnfusedCall:
+    """The unfused baseline with its arguments marshalled once: calling it
+    launches tw_reduce_partials into ``out`` and then tw_add_rmsnorm over
+    ``out`` in place (two launches)."""
+
+    def __init__(self, partials, residual, gamma, eps, out, stream=None):
+        arr, n = _partials_array(partials)
+        T, H = _shape(residual)
+        self.tensors = (partials, residual, gamma, out)
+        L = lib()
+        s = _stream(stream)
+        self._reduce = (L.tw_reduce_partials, (arr, n, T, H, _ptr(out), s))
+        self._norm = (L.tw_add_rmsnorm, (_ptr(out), _ptr(residual), _ptr(gamma),
+                                         ctypes.c_float(eps), T, H, _ptr(out), s))
+
+    def __call__(self):
+        for fn, args in (self._reduce, self._norm):
+            st = fn(*args)
+            if st != TW_OK:
+                raise TwError(st, fn.__name__)
 
 
 def tw_launch_shape(T, H, N, sm_budget=0):

@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "libtw")
 LIB = os.path.join(PKG, "libtw.so")
 
-SOURCES = ["fused_kernel.cu", "abi.cpp", "planner.cpp"]
+SOURCES = ["fused_kernel.cu", "unfused_kernels.cu", "abi.cpp", "planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "-I", INCLUDE, "-I", CSRC] + ARCH

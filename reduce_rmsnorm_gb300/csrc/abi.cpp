@@ -162,6 +162,45 @@ extern "C" int tw_run_split(int64_t prefix_tokens, const void* const* partials, 
   }
 }
 
+extern "C" int tw_reduce_partials(const void* const* partials, int N, int64_t T, int64_t H,
+                                  void* sum_out, tw_stream_t stream) {
+  try {
+    int st = validate_shape(N, 0.0f, T, H, 0);
+    if (st != TW_OK || T == 0) return st;
+    if (!partials || !sum_out) return TW_ERR_INVALID_ARG;
+    for (int r = 0; r < N; ++r)
+      if (!partials[r]) return TW_ERR_INVALID_ARG;
+    for (int r = 0; r < N; ++r)
+      if (!aligned16(partials[r])) return TW_ERR_ALIGN;
+    if (!aligned16(sum_out)) return TW_ERR_ALIGN;
+    const int64_t bytes = T * H * 2;
+    for (int r = 0; r < N; ++r)
+      if (overlap(sum_out, partials[r], bytes)) return TW_ERR_INVALID_ARG;
+    return tw::launch_reduce(partials, N, T, H, sum_out, reinterpret_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
+extern "C" int tw_add_rmsnorm(const void* sum, void* residual, const void* gamma, float eps,
+                              int64_t T, int64_t H, void* out, tw_stream_t stream) {
+  try {
+    int st = validate_shape(1, eps, T, H, 0);
+    if (st != TW_OK || T == 0) return st;
+    if (!sum || !residual || !gamma || !out) return TW_ERR_INVALID_ARG;
+    if (!aligned16(sum) || !aligned16(residual) || !aligned16(gamma) || !aligned16(out))
+      return TW_ERR_ALIGN;
+    const int64_t bytes = T * H * 2;
+    if (overlap(residual, out, bytes) || overlap(residual, sum, bytes)) return TW_ERR_INVALID_ARG;
+    if (overlap(residual, gamma, H * 2) || overlap(out, gamma, H * 2)) return TW_ERR_INVALID_ARG;
+    if (sum != out && overlap(sum, out, bytes)) return TW_ERR_INVALID_ARG;  // same buffer is fine
+    return tw::launch_add_rmsnorm(sum, residual, gamma, eps, T, H, out,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
 extern "C" int tw_launch_shape(int64_t T, int64_t H, int N, int sm_budget, int* grid, int* threads,
                                int* smem_bytes, int* stages) {
   try {

@@ -36,6 +36,13 @@ int plan_launch(int64_t rows, int64_t hidden, int n, int sm_budget, LaunchShape*
 // Enqueue the fused kernel on `stream`. smid_out: optional device int32[grid].
 int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* smid_out);
 
+// Unfused baseline (unfused_kernels.cu): S = bf16(sum of partials), then the
+// residual add + RMSNorm of the stored residual.
+int launch_reduce(const void* const* partials, int n, int64_t rows, int64_t hidden, void* sum,
+                  cudaStream_t stream);
+int launch_add_rmsnorm(const void* sum, void* residual, const void* gamma, float eps, int64_t rows,
+                       int64_t hidden, void* out, cudaStream_t stream);
+
 // Read (and optionally clear) the device-side error word of the current device.
 int read_device_error(int reset, int* code);
 
