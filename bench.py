@@ -3,6 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...      # the CPU oracle, timed on host cores
     python bench.py --sweep                   # SM-budget x token-count table (many lines)
+    python bench.py --corun                   # split pipelined against a GEMM (many lines)
 
 A step is one pass of the hot path over one batch: the wave-aware split plan
 (tw_wave_split, host) and the fused step over the batch (tw_run_split: prefix
@@ -519,6 +520,136 @@ def sweep(args):
     assert tw.tw_device_status(reset=True) == 0
 
 
+# ------------------------------------------------------------------ co-run with a GEMM
+
+
+def corun(args):
+    """The split pipelined against the projection that produces the partials
+    (one JSON line per token count and SM budget):
+
+      serial    GEMM(T) then the fused step on the whole GPU, one stream
+      overlap   stream A: GEMM(prefix), GEMM(suffix); stream B (high priority,
+                sm_budget): fused(prefix) after GEMM(prefix), fused(suffix)
+                after GEMM(suffix) (tw_run_split_after); planner split
+      equal     the same with prefix = T/2
+      model     T_GEMM(p) + max(T_GEMM(T-p), T_FUSED(p)) + T_FUSED(T-p), the
+                overlap formula of the pages' guide, from the pieces timed alone
+      gemm_slowdown   GEMM(T) time while a long fused call runs at the budget,
+                      over GEMM(T) alone
+
+    The GEMM is a row-parallel down projection of one rank, [T, 4H/N] x
+    [4H/N, H] in bf16 (torch.matmul, cuBLAS), writing partial 0; partials
+    1..N-1 stand for the other ranks' contributions already in HBM."""
+    import torch
+    import reduce_rmsnorm_gb300 as tw
+    import synth
+    from reduce_rmsnorm_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    H, N, eps = 8192, 8, 1e-5
+    K = 4 * H // N
+    sa = torch.cuda.Stream(dev, priority=0)
+    sb = torch.cuda.Stream(dev, priority=-1)
+    gen = torch.Generator(device=dev).manual_seed(0)
+    reps = args.corun_reps
+
+    def timed(fn, stream):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        out = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            out.append(a.elapsed_time(b) * 1e3)
+        return sorted(out)[len(out) // 2]
+
+    for T in [int(t) for t in args.corun_tokens.split(",")]:
+        p_cpu, r_cpu, g_cpu = synth.make_inputs(T, H, N, 0.02, seed=T)
+        P, R, G = p_cpu.to(dev), r_cpu.to(dev), g_cpu.to(dev)
+        x = torch.randn((T, K), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        w = (torch.randn((K, H), generator=gen, device=dev, dtype=torch.float32)
+             * K ** -0.5).to(torch.bfloat16)
+        out = torch.empty_like(R)
+        C = ctas_unsplit(T, H)
+        plan_p = tw.tw_wave_split(T, C, PLANNER_SMS)[0]
+        cover = synth.make_inputs(4096, H, N, 0.02, seed=1)
+        Pc, Rc, Gc = cover[0].to(dev), cover[1].to(dev), cover[2].to(dev)
+        outc = torch.empty_like(Rc)
+        torch.cuda.synchronize()
+
+        def gemm(a, b):
+            if b > a:
+                torch.matmul(x[a:b], w, out=P[0, a:b])
+
+        for budget in [int(b) for b in args.corun_budgets.split(",")]:
+            def serial():
+                with torch.cuda.stream(sa):
+                    gemm(0, T)
+                    tw.tw_fused_reduce_residual_rmsnorm(P, R, G, eps, out, stream=sa)
+
+            def overlap(p):
+                def run():
+                    e1, e2 = torch.cuda.Event(), torch.cuda.Event()
+                    sb.wait_stream(sa)
+                    with torch.cuda.stream(sa):
+                        gemm(0, p)
+                        e1.record(sa)
+                        gemm(p, T)
+                        e2.record(sa)
+                    tw.tw_run_split_after(p, P, R, G, eps, out, sb, e1, e2, sm_budget=budget)
+                    sa.wait_stream(sb)
+                return run
+
+            def fused_rows(a, b):
+                def run():
+                    if b > a:
+                        tw.tw_fused_reduce_residual_rmsnorm(P[:, a:b], R[a:b], G, eps, out[a:b],
+                                                            stream=sa, sm_budget=budget)
+                return run
+
+            def gemm_rows(a, b):
+                def run():
+                    with torch.cuda.stream(sa):
+                        gemm(a, b)
+                return run
+
+            def gemm_beside_fused():
+                sb.wait_stream(sa)
+                tw.tw_fused_reduce_residual_rmsnorm(Pc, Rc, Gc, eps, outc, stream=sb,
+                                                    sm_budget=budget)
+                with torch.cuda.stream(sa):
+                    gemm(0, T)
+
+            t_serial = timed(serial, sa)
+            t_overlap = timed(overlap(plan_p), sa)
+            t_equal = timed(overlap(T // 2), sa)
+            g_p, g_s = timed(gemm_rows(0, plan_p), sa), timed(gemm_rows(plan_p, T), sa)
+            f_p, f_s = timed(fused_rows(0, plan_p), sa), timed(fused_rows(plan_p, T), sa)
+            g_all = timed(gemm_rows(0, T), sa)
+            g_beside = timed(gemm_beside_fused, sa) if budget else None
+            torch.cuda.synchronize()
+            model = g_p + max(g_s, f_p) + f_s
+            print(json.dumps({
+                "T": T, "H": H, "N": N, "gemm": "[%d,%d]x[%d,%d] bf16" % (T, K, K, H),
+                "sm_budget": budget or "full", "plan": [plan_p, T - plan_p],
+                "serial_us": round(t_serial, 2), "overlap_us": round(t_overlap, 2),
+                "equal_split_us": round(t_equal, 2),
+                "speedup_vs_serial": round(t_serial / t_overlap, 3),
+                "model_us": round(model, 2),
+                "pieces_us": {"gemm_prefix": round(g_p, 2), "gemm_suffix": round(g_s, 2),
+                              "fused_prefix": round(f_p, 2), "fused_suffix": round(f_s, 2),
+                              "gemm_all": round(g_all, 2)},
+                "gemm_slowdown": None if g_beside is None else round(g_beside / g_all, 3)}),
+                flush=True)
+        del P, R, G, x, w, out, Pc, Rc, Gc, outc
+        torch.cuda.empty_cache()
+    assert tw.tw_device_status(reset=True) == 0
+
+
 # ------------------------------------------------------------------ main
 
 
@@ -539,12 +670,19 @@ def main(argv=None):
     ap.add_argument("--sweep-tokens", default="512,1024,2048,4096,8192,16384")
     ap.add_argument("--sweep-budgets", default="2,4,8,16,0")
     ap.add_argument("--sweep-reps", type=int, default=50)
+    ap.add_argument("--corun", action="store_true")
+    ap.add_argument("--corun-tokens", default="1024,2048,4096,8192")
+    ap.add_argument("--corun-budgets", default="2,4,8,16,0")
+    ap.add_argument("--corun-reps", type=int, default=20)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     if args.sweep:
         sweep(args)
+        return
+    if args.corun:
+        corun(args)
         return
     if args.impl == "reference":
         # rank 0 alone times the oracle; other ranks exit without work

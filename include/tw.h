@@ -31,6 +31,8 @@ extern "C" {
 
 struct CUstream_st;
 typedef struct CUstream_st* tw_stream_t; /* == cudaStream_t */
+struct CUevent_st;
+typedef struct CUevent_st* tw_event_t; /* == cudaEvent_t */
 
 /* Largest number of partial buffers (tensor-parallel ranks) one call sums. */
 #define TW_MAX_PARTIALS 16
@@ -162,6 +164,28 @@ int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_sms, const t
 int tw_run_split(int64_t prefix_tokens, const void* const* partials, int N, void* residual,
                  const void* gamma, float eps, int64_t T, int64_t H, void* out,
                  tw_stream_t stream_a, tw_stream_t stream_b, int sm_budget);
+
+/*
+ * tw_run_split_after -- the split step as the pages pipeline it against the
+ * projection that produces the partials ([G] "Architectural Foundations of
+ * TokenWeave" and "The Mathematics of Token-Splitting and Overlap": stream A
+ * computes GEMM(T1) then GEMM(T2); stream B runs the fused step of T1 as soon
+ * as GEMM(T1) is done, overlapping GEMM(T2), then the fused step of T2).
+ *
+ * On `stream`, in order: wait for `prefix_ready` (if not NULL), run the
+ * fused step on rows [0, prefix_tokens); wait for `suffix_ready` (if not
+ * NULL), run it on rows [prefix_tokens, T). The caller records the events on
+ * the stream that produces the prefix's and the suffix's partials. Give
+ * `stream` a high priority so its CTAs are placed ahead of the compute
+ * kernel's as SMs free up, and an sm_budget so the compute keeps the rest.
+ * The result is bitwise that of the unsplit call. Empty halves are skipped.
+ * Arguments and errors as for tw_run_split; events are cudaEvent_t handles
+ * owned by the caller.
+ */
+int tw_run_split_after(int64_t prefix_tokens, const void* const* partials, int N, void* residual,
+                       const void* gamma, float eps, int64_t T, int64_t H, void* out,
+                       tw_stream_t stream, tw_event_t prefix_ready, tw_event_t suffix_ready,
+                       int sm_budget);
 
 /* Text of a tw_status value (static storage; never NULL). */
 const char* tw_strerror(int status);

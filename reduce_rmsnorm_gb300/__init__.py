@@ -10,6 +10,8 @@ The functions carry the C names:
     tw_fused_reduce_residual_rmsnorm(partials, residual, gamma, eps, out, stream=None, sm_budget=0)
     tw_wave_split(num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS, min_split_tokens=1024)
     tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a, stream_b, sm_budget=0)
+    tw_run_split_after(prefix_tokens, partials, residual, gamma, eps, out, stream,
+                       prefix_ready, suffix_ready, sm_budget=0)
     tw_strerror(status)
     tw_launch_shape(T, H, N, sm_budget=0)
     tw_device_status(reset=True)
@@ -41,7 +43,7 @@ DEFAULT_MIN_SPLIT_TOKENS = 1024
 
 EXPORTED = ("tw_fused_reduce_residual_rmsnorm", "tw_wave_split", "tw_run_split", "tw_strerror",
             "tw_launch_shape", "tw_device_status", "tw_fused_debug_smid", "tw_reduce_partials",
-            "tw_add_rmsnorm")
+            "tw_add_rmsnorm", "tw_run_split_after")
 
 
 class TwError(RuntimeError):
@@ -90,6 +92,9 @@ def lib():
     L.tw_launch_shape.restype = _int
     L.tw_device_status.argtypes = [_int, ctypes.POINTER(_int)]
     L.tw_device_status.restype = _int
+    L.tw_run_split_after.argtypes = [_i64, ctypes.POINTER(_vp), _int, _vp, _vp, ctypes.c_float,
+                                     _i64, _i64, _vp, _vp, _vp, _vp, _int]
+    L.tw_run_split_after.restype = _int
     L.tw_reduce_partials.argtypes = [ctypes.POINTER(_vp), _int, _i64, _i64, _vp, _vp]
     L.tw_reduce_partials.restype = _int
     L.tw_add_rmsnorm.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp]
@@ -192,6 +197,23 @@ def tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a=No
     st = lib().tw_run_split(int(prefix_tokens), arr, n, _ptr(residual), _ptr(gamma), float(eps), T,
                             H, _ptr(out), _stream(stream_a), _stream(stream_b), int(sm_budget))
     _check(st, "tw_run_split")
+
+
+def _event(e):
+    return None if e is None else ctypes.c_void_p(e.cuda_event if hasattr(e, "cuda_event") else int(e))
+
+
+def tw_run_split_after(prefix_tokens, partials, residual, gamma, eps, out, stream=None,
+                       prefix_ready=None, suffix_ready=None, sm_budget=0):
+    """On `stream`: wait prefix_ready, fused step on rows [0, prefix); wait
+    suffix_ready, fused step on rows [prefix, T). Events: torch.cuda.Event or
+    raw cudaEvent_t handles."""
+    arr, n = _partials_array(partials)
+    T, H = _shape(residual)
+    st = lib().tw_run_split_after(int(prefix_tokens), arr, n, _ptr(residual), _ptr(gamma),
+                                  float(eps), T, H, _ptr(out), _stream(stream),
+                                  _event(prefix_ready), _event(suffix_ready), int(sm_budget))
+    _check(st, "tw_run_split_after")
 
 
 def tw_reduce_partials(partials, sum_out, stream=None):

@@ -162,6 +162,34 @@ extern "C" int tw_run_split(int64_t prefix_tokens, const void* const* partials, 
   }
 }
 
+extern "C" int tw_run_split_after(int64_t prefix_tokens, const void* const* partials, int N,
+                                  void* residual, const void* gamma, float eps, int64_t T,
+                                  int64_t H, void* out, tw_stream_t stream, tw_event_t prefix_ready,
+                                  tw_event_t suffix_ready, int sm_budget) {
+  try {
+    tw::FusedArgs a;
+    int st = validate(partials, N, residual, gamma, eps, T, H, out, sm_budget, &a);
+    if (st != TW_OK) return st;
+    if (prefix_tokens < 0 || prefix_tokens > T) return TW_ERR_INVALID_ARG;
+    if (T == 0) return TW_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t suffix = T - prefix_tokens;
+    if (prefix_ready &&
+        cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(prefix_ready), 0) != cudaSuccess)
+      return TW_ERR_CUDA;
+    if (prefix_tokens > 0 &&
+        (st = tw::launch_fused(slice(a, 0, prefix_tokens), s, sm_budget, nullptr)) != TW_OK)
+      return st;
+    if (suffix_ready &&
+        cudaStreamWaitEvent(s, reinterpret_cast<cudaEvent_t>(suffix_ready), 0) != cudaSuccess)
+      return TW_ERR_CUDA;
+    if (suffix > 0) return tw::launch_fused(slice(a, prefix_tokens, suffix), s, sm_budget, nullptr);
+    return TW_OK;
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
 extern "C" int tw_reduce_partials(const void* const* partials, int N, int64_t T, int64_t H,
                                   void* sum_out, tw_stream_t stream) {
   try {
