@@ -19,8 +19,8 @@
 //     the N + 1 copies of a stage go out in parallel (one lane issuing them in
 //     turn, or 4 KiB copies, caps an SM near 45 GB/s). Eight consumer warps
 //     read a chunk (one or two 16-byte vectors per thread per source), sum in
-//     fp32 in rank order, add the residual, store the updated residual, and
-//     keep z in registers.
+//     fp32 in rank order (packed f32x2 adds), add the residual, store the
+//     updated residual, and keep z in registers.
 //   * After a row's last chunk: warp xor-shuffle sum of squares, a fixed-order
 //     combine of the 8 warp sums, rsqrtf, and Y = (z * r) * gamma stored with
 //     16-byte stores. The per-row arithmetic depends only on H, so every grid
@@ -203,11 +203,22 @@ __device__ __forceinline__ void load8(const uint4 q, float a[8]) {
   a[6] = bf16_lo(q.w); a[7] = bf16_hi(q.w);
 }
 
+// a[2i], a[2i+1] += the two bf16 values of word w, as one packed fp32x2 add
+// (add.rn.f32x2: two independent IEEE round-to-nearest fp32 additions, the
+// same results as two scalar adds, in one instruction).
+__device__ __forceinline__ void add2(float& lo, float& hi, uint32_t w) {
+  uint64_t acc, v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(lo), "f"(hi));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(w << 16), "r"(w & 0xffff0000u));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(v));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc));
+}
+
 __device__ __forceinline__ void add8(const uint4 q, float a[8]) {
-  a[0] += bf16_lo(q.x); a[1] += bf16_hi(q.x);
-  a[2] += bf16_lo(q.y); a[3] += bf16_hi(q.y);
-  a[4] += bf16_lo(q.z); a[5] += bf16_hi(q.z);
-  a[6] += bf16_lo(q.w); a[7] += bf16_hi(q.w);
+  add2(a[0], a[1], q.x);
+  add2(a[2], a[3], q.y);
+  add2(a[4], a[5], q.z);
+  add2(a[6], a[7], q.w);
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
