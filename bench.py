@@ -4,6 +4,7 @@
     python bench.py --impl reference ...      # the CPU oracle, timed on host cores
     python bench.py --sweep                   # SM-budget x token-count table (many lines)
     python bench.py --corun                   # split pipelined against a GEMM (many lines)
+    python bench.py --offset-sweep [--sm-budget k]   # timed offset sweep -> lookup table
 
 A step is one pass of the hot path over one batch: the wave-aware split plan
 (tw_wave_split, host) and the fused step over the batch (tw_run_split: prefix
@@ -523,118 +524,139 @@ def sweep(args):
 # ------------------------------------------------------------------ co-run with a GEMM
 
 
-def corun(args):
-    """The split pipelined against the projection that produces the partials
-    (one JSON line per token count and SM budget):
+class GemmPipeline:
+    """One tensor-parallel layer's tail on one GPU: the row-parallel down
+    projection of one rank, [T, 4H/N] x [4H/N, H] in bf16 (torch.matmul,
+    cuBLAS), writes partial 0; partials 1..N-1 stand for the other ranks'
+    contributions already in HBM. forward(prefix) runs, as the pages' guide
+    pipelines it:
 
-      serial    GEMM(T) then the fused step on the whole GPU, one stream
-      overlap   stream A: GEMM(prefix), GEMM(suffix); stream B (high priority,
-                sm_budget): fused(prefix) after GEMM(prefix), fused(suffix)
-                after GEMM(suffix) (tw_run_split_after); planner split
-      equal     the same with prefix = T/2
-      model     T_GEMM(p) + max(T_GEMM(T-p), T_FUSED(p)) + T_FUSED(T-p), the
-                overlap formula of the pages' guide, from the pieces timed alone
-      gemm_slowdown   GEMM(T) time while a long fused call runs at the budget,
-                      over GEMM(T) alone
+      stream A (compute):            GEMM(rows [0,p)) -> GEMM(rows [p,T))
+      stream B (high priority, k SMs): fused(rows [0,p)) after GEMM(prefix),
+                                     fused(rows [p,T)) after GEMM(suffix)
 
-    The GEMM is a row-parallel down projection of one rank, [T, 4H/N] x
-    [4H/N, H] in bf16 (torch.matmul, cuBLAS), writing partial 0; partials
-    1..N-1 stand for the other ranks' contributions already in HBM."""
-    import torch
-    import reduce_rmsnorm_gb300 as tw
-    import synth
-    from reduce_rmsnorm_gb300 import build
-    build.build()
-    dev = torch.device("cuda", 0)
-    H, N, eps = 8192, 8, 1e-5
-    K = 4 * H // N
-    sa = torch.cuda.Stream(dev, priority=0)
-    sb = torch.cuda.Stream(dev, priority=-1)
-    gen = torch.Generator(device=dev).manual_seed(0)
-    reps = args.corun_reps
+    prefix == T is the unsplit forward: GEMM(T) then the fused step."""
 
-    def timed(fn, stream):
+    def __init__(self, T, H=8192, N=8, sm_budget=0, seed=0):
+        import torch
+        import synth
+        dev = torch.device("cuda", 0)
+        self.T, self.H, self.N, self.budget, self.eps = T, H, N, sm_budget, 1e-5
+        K = 4 * H // N
+        p, r, g = synth.make_inputs(T, H, N, 0.02, seed=seed)
+        self.P, self.R, self.G = p.to(dev), r.to(dev), g.to(dev)
+        gen = torch.Generator(device=dev).manual_seed(seed)
+        self.x = torch.randn((T, K), generator=gen, device=dev).to(torch.bfloat16)
+        self.w = (torch.randn((K, H), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
+        self.out = torch.empty_like(self.R)
+        self.sa = torch.cuda.Stream(dev, priority=0)
+        self.sb = torch.cuda.Stream(dev, priority=-1)
+        self.gemm_shape = "[%d,%d]x[%d,%d] bf16" % (T, K, K, H)
+        torch.cuda.synchronize()
+
+    def gemm(self, a, b):
+        import torch
+        if b > a:
+            torch.matmul(self.x[a:b], self.w, out=self.P[0, a:b])
+
+    def forward(self, prefix):
+        import torch
+        import reduce_rmsnorm_gb300 as tw
+        sa, sb = self.sa, self.sb
+        e1, e2 = torch.cuda.Event(), torch.cuda.Event()
+        sb.wait_stream(sa)
+        with torch.cuda.stream(sa):
+            self.gemm(0, prefix)
+            e1.record(sa)
+            self.gemm(prefix, self.T)
+            e2.record(sa)
+        tw.tw_run_split_after(prefix, self.P, self.R, self.G, self.eps, self.out, sb, e1, e2,
+                              sm_budget=self.budget)
+        sa.wait_stream(sb)
+
+    def serial(self):
+        import torch
+        import reduce_rmsnorm_gb300 as tw
+        with torch.cuda.stream(self.sa):
+            self.gemm(0, self.T)
+            tw.tw_fused_reduce_residual_rmsnorm(self.P, self.R, self.G, self.eps, self.out,
+                                                stream=self.sa)
+
+    def timed(self, fn, reps):
+        """Median microseconds of fn() on stream A (events on A; A joins B)."""
+        import torch
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
         out = []
         for _ in range(reps):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
+            a.record(self.sa)
             fn()
-            b.record(stream)
+            b.record(self.sa)
             torch.cuda.synchronize()
             out.append(a.elapsed_time(b) * 1e3)
         return sorted(out)[len(out) // 2]
 
+
+def corun(args):
+    """The split pipelined against the projection that produces the partials
+    (one JSON line per token count and SM budget):
+
+      serial    GEMM(T) then the fused step on the whole GPU, one stream
+      overlap   GemmPipeline.forward with the planner's split at the budget
+      equal     the same with prefix = T/2
+      model     T_GEMM(p) + max(T_GEMM(T-p), T_FUSED(p)) + T_FUSED(T-p), the
+                overlap formula of the pages' guide, from the pieces timed alone
+      gemm_slowdown   GEMM(T) time while a long fused call runs at the budget,
+                      over GEMM(T) alone"""
+    import torch
+    import reduce_rmsnorm_gb300 as tw
+    import synth
+    from reduce_rmsnorm_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    reps = args.corun_reps
+    cover = synth.make_inputs(4096, 8192, 8, 0.02, seed=1)
+    Pc, Rc, Gc = cover[0].to(dev), cover[1].to(dev), cover[2].to(dev)
+    outc = torch.empty_like(Rc)
     for T in [int(t) for t in args.corun_tokens.split(",")]:
-        p_cpu, r_cpu, g_cpu = synth.make_inputs(T, H, N, 0.02, seed=T)
-        P, R, G = p_cpu.to(dev), r_cpu.to(dev), g_cpu.to(dev)
-        x = torch.randn((T, K), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
-        w = (torch.randn((K, H), generator=gen, device=dev, dtype=torch.float32)
-             * K ** -0.5).to(torch.bfloat16)
-        out = torch.empty_like(R)
-        C = ctas_unsplit(T, H)
-        plan_p = tw.tw_wave_split(T, C, PLANNER_SMS)[0]
-        cover = synth.make_inputs(4096, H, N, 0.02, seed=1)
-        Pc, Rc, Gc = cover[0].to(dev), cover[1].to(dev), cover[2].to(dev)
-        outc = torch.empty_like(Rc)
-        torch.cuda.synchronize()
-
-        def gemm(a, b):
-            if b > a:
-                torch.matmul(x[a:b], w, out=P[0, a:b])
-
         for budget in [int(b) for b in args.corun_budgets.split(",")]:
-            def serial():
-                with torch.cuda.stream(sa):
-                    gemm(0, T)
-                    tw.tw_fused_reduce_residual_rmsnorm(P, R, G, eps, out, stream=sa)
-
-            def overlap(p):
-                def run():
-                    e1, e2 = torch.cuda.Event(), torch.cuda.Event()
-                    sb.wait_stream(sa)
-                    with torch.cuda.stream(sa):
-                        gemm(0, p)
-                        e1.record(sa)
-                        gemm(p, T)
-                        e2.record(sa)
-                    tw.tw_run_split_after(p, P, R, G, eps, out, sb, e1, e2, sm_budget=budget)
-                    sa.wait_stream(sb)
-                return run
+            pipe = GemmPipeline(T, sm_budget=budget, seed=T)
+            C = ctas_unsplit(T, pipe.H)
+            plan_p = tw.tw_wave_split(T, C, PLANNER_SMS)[0]
 
             def fused_rows(a, b):
                 def run():
                     if b > a:
-                        tw.tw_fused_reduce_residual_rmsnorm(P[:, a:b], R[a:b], G, eps, out[a:b],
-                                                            stream=sa, sm_budget=budget)
+                        tw.tw_fused_reduce_residual_rmsnorm(
+                            pipe.P[:, a:b], pipe.R[a:b], pipe.G, pipe.eps, pipe.out[a:b],
+                            stream=pipe.sa, sm_budget=budget)
                 return run
 
             def gemm_rows(a, b):
                 def run():
-                    with torch.cuda.stream(sa):
-                        gemm(a, b)
+                    with torch.cuda.stream(pipe.sa):
+                        pipe.gemm(a, b)
                 return run
 
             def gemm_beside_fused():
-                sb.wait_stream(sa)
-                tw.tw_fused_reduce_residual_rmsnorm(Pc, Rc, Gc, eps, outc, stream=sb,
+                pipe.sb.wait_stream(pipe.sa)
+                tw.tw_fused_reduce_residual_rmsnorm(Pc, Rc, Gc, pipe.eps, outc, stream=pipe.sb,
                                                     sm_budget=budget)
-                with torch.cuda.stream(sa):
-                    gemm(0, T)
+                with torch.cuda.stream(pipe.sa):
+                    pipe.gemm(0, T)
 
-            t_serial = timed(serial, sa)
-            t_overlap = timed(overlap(plan_p), sa)
-            t_equal = timed(overlap(T // 2), sa)
-            g_p, g_s = timed(gemm_rows(0, plan_p), sa), timed(gemm_rows(plan_p, T), sa)
-            f_p, f_s = timed(fused_rows(0, plan_p), sa), timed(fused_rows(plan_p, T), sa)
-            g_all = timed(gemm_rows(0, T), sa)
-            g_beside = timed(gemm_beside_fused, sa) if budget else None
-            torch.cuda.synchronize()
+            t_serial = pipe.timed(pipe.serial, reps)
+            t_overlap = pipe.timed(lambda: pipe.forward(plan_p), reps)
+            t_equal = pipe.timed(lambda: pipe.forward(T // 2), reps)
+            g_p, g_s = pipe.timed(gemm_rows(0, plan_p), reps), pipe.timed(gemm_rows(plan_p, T), reps)
+            f_p, f_s = pipe.timed(fused_rows(0, plan_p), reps), pipe.timed(fused_rows(plan_p, T), reps)
+            g_all = pipe.timed(gemm_rows(0, T), reps)
+            g_beside = pipe.timed(gemm_beside_fused, reps) if budget else None
             model = g_p + max(g_s, f_p) + f_s
             print(json.dumps({
-                "T": T, "H": H, "N": N, "gemm": "[%d,%d]x[%d,%d] bf16" % (T, K, K, H),
+                "T": T, "H": pipe.H, "N": pipe.N, "gemm": pipe.gemm_shape,
                 "sm_budget": budget or "full", "plan": [plan_p, T - plan_p],
                 "serial_us": round(t_serial, 2), "overlap_us": round(t_overlap, 2),
                 "equal_split_us": round(t_equal, 2),
@@ -645,8 +667,50 @@ def corun(args):
                               "gemm_all": round(g_all, 2)},
                 "gemm_slowdown": None if g_beside is None else round(g_beside / g_all, 3)}),
                 flush=True)
-        del P, R, G, x, w, out, Pc, Rc, Gc, outc
+            del pipe
+            torch.cuda.empty_cache()
+    assert tw.tw_device_status(reset=True) == 0
+
+
+def offset_sweep(args):
+    """The pages' offline selection rule ("Fix one" of the wave-arithmetic
+    blog): for each token count, time a forward for every candidate split
+    (no split, and half -/+ each offset of the grid below half), keep the
+    fastest as the lookup table's entry, and compare it with the planner's
+    wave-constraint choice. One JSON line per token count, then the table."""
+    import torch
+    import reduce_rmsnorm_gb300 as tw
+    from reduce_rmsnorm_gb300 import build
+    build.build()
+    table = {}
+    agree = 0
+    tokens = [int(t) for t in args.sweep_offsets_tokens.split(",")]
+    for T in tokens:
+        pipe = GemmPipeline(T, sm_budget=args.sm_budget, seed=T)
+        half = T // 2
+        cands = [T] + sorted({half - o for o in tw.DEFAULT_OFFSETS if o < half} |
+                             {half + o for o in tw.DEFAULT_OFFSETS if o < half})
+        times = {p: pipe.timed(lambda p=p: pipe.forward(p), args.corun_reps) for p in cands}
+        # fastest; ties (within 0.5%) go to the smaller |p - half|, then the smaller prefix
+        best_t = min(times.values())
+        best = min((p for p in cands if times[p] <= best_t * 1.005),
+                   key=lambda p: (abs(p - half) if p != T else T, p))
+        plan = tw.tw_wave_split(T, ctas_unsplit(T, pipe.H), PLANNER_SMS)[0]
+        agree += int(plan == best)
+        table[T] = best
+        print(json.dumps({"T": T, "sm_budget": args.sm_budget or "full",
+                          "table_prefix": best, "table_us": round(times[best], 2),
+                          "planner_prefix": plan, "planner_us": round(times[plan], 2)
+                          if plan in times else None,
+                          "planner_loss": round(times[plan] / times[best], 4)
+                          if plan in times else None,
+                          "equal_us": round(times[half], 2), "unsplit_us": round(times[T], 2),
+                          "candidates_us": {str(p): round(t, 2) for p, t in sorted(times.items())}}),
+              flush=True)
+        del pipe
         torch.cuda.empty_cache()
+    print(json.dumps({"table": {str(k): v for k, v in table.items()},
+                      "planner_agrees": agree, "of": len(tokens)}), flush=True)
     assert tw.tw_device_status(reset=True) == 0
 
 
@@ -674,6 +738,9 @@ def main(argv=None):
     ap.add_argument("--corun-tokens", default="1024,2048,4096,8192")
     ap.add_argument("--corun-budgets", default="2,4,8,16,0")
     ap.add_argument("--corun-reps", type=int, default=20)
+    ap.add_argument("--offset-sweep", action="store_true")
+    ap.add_argument("--sweep-offsets-tokens",
+                    default="1024,1536,2048,2560,3072,3584,4096,4864,5376,6144,7168,8192,9600")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -683,6 +750,9 @@ def main(argv=None):
         return
     if args.corun:
         corun(args)
+        return
+    if args.offset_sweep:
+        offset_sweep(args)
         return
     if args.impl == "reference":
         # rank 0 alone times the oracle; other ranks exit without work

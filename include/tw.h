@@ -141,6 +141,27 @@ int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_sms, const t
                   int64_t* prefix_tokens, int64_t* suffix_tokens);
 
 /*
+ * tw_split_lookup -- the split plan from a lookup table of measured splits,
+ * falling back to tw_wave_split.
+ *
+ * [W] "Fix one": because the GEMM kernels are closed, the split offset is
+ * chosen offline by timing a forward pass for each offset and storing the
+ * winner per token count in a lookup table, consulted every iteration. The
+ * table here is n_entries pairs (table_tokens[i], table_prefix[i]), e.g. as
+ * written by `bench.py --offset-sweep`. If num_tokens equals table_tokens[i]
+ * for some i, the plan is (table_prefix[i], num_tokens - table_prefix[i]);
+ * otherwise it is tw_wave_split(num_tokens, ctas_unsplit, num_sms, opts).
+ * The first matching entry wins. Host-only integer code.
+ *
+ * Errors: TW_ERR_INVALID_ARG (n_entries < 0, a NULL table with n_entries >
+ * 0, a matching entry whose prefix is outside [0, num_tokens], or any error
+ * of tw_wave_split).
+ */
+int tw_split_lookup(const int64_t* table_tokens, const int64_t* table_prefix, int n_entries,
+                    int64_t num_tokens, int64_t ctas_unsplit, int num_sms,
+                    const tw_split_opts* opts, int64_t* prefix_tokens, int64_t* suffix_tokens);
+
+/*
  * tw_run_split -- the fused step over a token batch split in two, on two
  * streams ([G] "Architectural Foundations of TokenWeave": the first chunk's
  * fused step runs on a second stream while the first stream goes on; [W]

@@ -9,6 +9,7 @@ The functions carry the C names:
 
     tw_fused_reduce_residual_rmsnorm(partials, residual, gamma, eps, out, stream=None, sm_budget=0)
     tw_wave_split(num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS, min_split_tokens=1024)
+    tw_split_lookup(table, num_tokens, ctas_unsplit, num_sms, offsets=..., min_split_tokens=...)
     tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a, stream_b, sm_budget=0)
     tw_run_split_after(prefix_tokens, partials, residual, gamma, eps, out, stream,
                        prefix_ready, suffix_ready, sm_budget=0)
@@ -43,7 +44,7 @@ DEFAULT_MIN_SPLIT_TOKENS = 1024
 
 EXPORTED = ("tw_fused_reduce_residual_rmsnorm", "tw_wave_split", "tw_run_split", "tw_strerror",
             "tw_launch_shape", "tw_device_status", "tw_fused_debug_smid", "tw_reduce_partials",
-            "tw_add_rmsnorm", "tw_run_split_after")
+            "tw_add_rmsnorm", "tw_run_split_after", "tw_split_lookup")
 
 
 class TwError(RuntimeError):
@@ -83,6 +84,10 @@ def lib():
     L.tw_wave_split.argtypes = [_i64, _i64, _int, ctypes.POINTER(_SplitOpts),
                                 ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
     L.tw_wave_split.restype = _int
+    L.tw_split_lookup.argtypes = [ctypes.POINTER(_i64), ctypes.POINTER(_i64), _int, _i64, _i64,
+                                  _int, ctypes.POINTER(_SplitOpts), ctypes.POINTER(_i64),
+                                  ctypes.POINTER(_i64)]
+    L.tw_split_lookup.restype = _int
     L.tw_run_split.argtypes = [_i64, ctypes.POINTER(_vp), _int, _vp, _vp, ctypes.c_float, _i64,
                                _i64, _vp, _vp, _vp, _int]
     L.tw_run_split.restype = _int
@@ -186,6 +191,29 @@ def tw_wave_split(num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS,
                              ctypes.byref(p), ctypes.byref(s))
     del keep
     _check(st, "tw_wave_split")
+    return p.value, s.value
+
+
+def _opts(offsets, min_split_tokens):
+    if offsets is None:
+        return _SplitOpts(None, 0, int(min_split_tokens)), None
+    keep = (ctypes.c_int * max(len(offsets), 1))(*[int(o) for o in offsets])
+    return _SplitOpts(keep, len(offsets), int(min_split_tokens)), keep
+
+
+def tw_split_lookup(table, num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS,
+                    min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
+    """(prefix, suffix) from ``table`` ({token count: prefix}) if it has the
+    token count, else from tw_wave_split."""
+    items = sorted(table.items())
+    toks = (_i64 * max(len(items), 1))(*[int(k) for k, _ in items])
+    pref = (_i64 * max(len(items), 1))(*[int(v) for _, v in items])
+    opts, keep = _opts(offsets, min_split_tokens)
+    p, s = _i64(), _i64()
+    st = lib().tw_split_lookup(toks, pref, len(items), int(num_tokens), int(ctas_unsplit),
+                               int(num_sms), ctypes.byref(opts), ctypes.byref(p), ctypes.byref(s))
+    del keep
+    _check(st, "tw_split_lookup")
     return p.value, s.value
 
 

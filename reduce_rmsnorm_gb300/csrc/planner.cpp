@@ -9,6 +9,9 @@
 // batches under the 1K-token threshold are not split. The worked example
 // (132 / 168 of 300 CTAs) puts the smaller piece first, so offsets are tried
 // with both signs, smallest |offset| first and the smaller prefix on a tie.
+// "Fix one" also describes the pages' own rule, an offline timed sweep whose
+// winners go in a lookup table; tw_split_lookup consults such a table and
+// falls back to the wave constraint.
 #include <algorithm>
 #include <cstdint>
 #include <vector>
@@ -87,4 +90,22 @@ extern "C" int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_s
     if (try_offset(off)) return TW_OK;
   }
   return TW_OK;
+}
+
+extern "C" int tw_split_lookup(const int64_t* table_tokens, const int64_t* table_prefix,
+                               int n_entries, int64_t num_tokens, int64_t ctas_unsplit,
+                               int num_sms, const tw_split_opts* opts, int64_t* prefix_tokens,
+                               int64_t* suffix_tokens) {
+  if (!prefix_tokens || !suffix_tokens || n_entries < 0) return TW_ERR_INVALID_ARG;
+  if (n_entries > 0 && (!table_tokens || !table_prefix)) return TW_ERR_INVALID_ARG;
+  if (num_tokens < 0) return TW_ERR_INVALID_ARG;
+  for (int i = 0; i < n_entries; ++i) {
+    if (table_tokens[i] != num_tokens) continue;
+    const int64_t p = table_prefix[i];
+    if (p < 0 || p > num_tokens) return TW_ERR_INVALID_ARG;
+    *prefix_tokens = p;
+    *suffix_tokens = num_tokens - p;
+    return TW_OK;
+  }
+  return tw_wave_split(num_tokens, ctas_unsplit, num_sms, opts, prefix_tokens, suffix_tokens);
 }

@@ -140,14 +140,12 @@ BASE = 0x7F0000000000  # fake device addresses; validation never dereferences th
 
 def _fused(L, N=2, T=4, H=16, eps=1e-5, sm_budget=0, partials=None, residual=None, gamma=None,
            out=None):
-    span = max(T * H * 2, 16) + 4096
     if partials is None:
         partials = [BASE + (r + 1) * (1 << 24) for r in range(N)]
     arr = (ctypes.c_void_p * max(len(partials), 1))(*partials)
     residual = BASE + (40 << 24) if residual is None else residual
     gamma = BASE + (41 << 24) if gamma is None else gamma
     out = BASE + (42 << 24) if out is None else out
-    del span
     return L.tw_fused_reduce_residual_rmsnorm(arr, N, residual, gamma, ctypes.c_float(eps), T, H,
                                               out, None, sm_budget)
 
@@ -227,3 +225,26 @@ def test_bytes_formula():
     assert tw.bytes_per_call(1024, 8192, 8) == 184_565_760
     assert tw.bytes_per_call(128, 4096, 2) == 5_251_072
     assert tw.bytes_per_call(8192, 16384, 8) == 2_952_822_784
+
+
+def test_split_lookup_table_then_planner(L):
+    table = {4096: 2112, 1000: 1000, 7168: 3456}
+    assert tw.tw_split_lookup(table, 4096, 256, 148) == (2112, 1984)
+    assert tw.tw_split_lookup(table, 1000, 600, 148) == (1000, 0)
+    # absent token counts fall back to the wave planner
+    for T in (8192, 4864, 1024, 0):
+        C = -(-T // 128) * 8
+        assert tw.tw_split_lookup(table, T, C, 148) == oplanner.wave_split(T, C, 148)
+    assert tw.tw_split_lookup({}, 4864, 304, 148) == (2368, 2496)
+
+
+def test_split_lookup_rejects_bad_tables(L):
+    with pytest.raises(tw.TwError):
+        tw.tw_split_lookup({4096: 5000}, 4096, 256, 148)     # prefix beyond T
+    with pytest.raises(tw.TwError):
+        tw.tw_split_lookup({4096: -1}, 4096, 256, 148)
+    p = ctypes.c_int64()
+    assert L.tw_split_lookup(None, None, 2, 10, 5, 4, None, ctypes.byref(p),
+                             ctypes.byref(ctypes.c_int64())) == tw.TW_ERR_INVALID_ARG
+    assert L.tw_split_lookup(None, None, -1, 10, 5, 4, None, ctypes.byref(p),
+                             ctypes.byref(ctypes.c_int64())) == tw.TW_ERR_INVALID_ARG
