@@ -231,6 +231,16 @@ int tw_launch_shape(int64_t T, int64_t H, int N, int sm_budget, int* grid, int* 
 int tw_device_status(int reset, int* code);
 
 /*
+ * tw_debug_wait_timeout -- a diagnostic of the kernels' bounded waits: one
+ * CTA waits, with the same bounded-wait routine the fused kernel uses, on a
+ * barrier phase that nothing completes. The wait gives up after limit_ns
+ * (1 us .. 2 s) and sets bit 0 of the device error word, which
+ * tw_device_status then reports. The GPU stays usable. For testing the
+ * failure path without faulting or hanging a GPU.
+ */
+int tw_debug_wait_timeout(int64_t limit_ns, tw_stream_t stream);
+
+/*
  * tw_fused_debug_smid -- the fused call, additionally writing the %smid of
  * each CTA to smid_out[blockIdx] (device int32 array with at least the
  * grid's length, see tw_launch_shape). For checking that an sm_budget of k

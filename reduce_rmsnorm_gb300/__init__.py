@@ -44,7 +44,7 @@ DEFAULT_MIN_SPLIT_TOKENS = 1024
 
 EXPORTED = ("tw_fused_reduce_residual_rmsnorm", "tw_wave_split", "tw_run_split", "tw_strerror",
             "tw_launch_shape", "tw_device_status", "tw_fused_debug_smid", "tw_reduce_partials",
-            "tw_add_rmsnorm", "tw_run_split_after", "tw_split_lookup")
+            "tw_add_rmsnorm", "tw_run_split_after", "tw_split_lookup", "tw_debug_wait_timeout")
 
 
 class TwError(RuntimeError):
@@ -84,6 +84,8 @@ def lib():
     L.tw_wave_split.argtypes = [_i64, _i64, _int, ctypes.POINTER(_SplitOpts),
                                 ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
     L.tw_wave_split.restype = _int
+    L.tw_debug_wait_timeout.argtypes = [_i64, _vp]
+    L.tw_debug_wait_timeout.restype = _int
     L.tw_split_lookup.argtypes = [ctypes.POINTER(_i64), ctypes.POINTER(_i64), _int, _i64, _i64,
                                   _int, ctypes.POINTER(_SplitOpts), ctypes.POINTER(_i64),
                                   ctypes.POINTER(_i64)]
@@ -329,6 +331,11 @@ def tw_launch_shape(T, H, N, sm_budget=0):
                                ctypes.byref(t), ctypes.byref(m), ctypes.byref(s))
     _check(st, "tw_launch_shape")
     return dict(grid=g.value, threads=t.value, smem_bytes=m.value, stages=s.value)
+
+
+def tw_debug_wait_timeout(limit_ns, stream=None):
+    """Diagnostic: a bounded wait that runs out after limit_ns (sets the error word)."""
+    _check(lib().tw_debug_wait_timeout(int(limit_ns), _stream(stream)), "tw_debug_wait_timeout")
 
 
 def tw_device_status(reset=True):

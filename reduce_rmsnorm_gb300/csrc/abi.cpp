@@ -256,6 +256,15 @@ extern "C" int tw_device_status(int reset, int* code) {
   }
 }
 
+extern "C" int tw_debug_wait_timeout(int64_t limit_ns, tw_stream_t stream) {
+  try {
+    if (limit_ns < 1000 || limit_ns > 2000000000ll) return TW_ERR_INVALID_ARG;
+    return tw::launch_wait_probe(limit_ns, reinterpret_cast<cudaStream_t>(stream));
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
 extern "C" const char* tw_strerror(int status) {
   switch (status) {
     case TW_OK: return "TW_OK: success";

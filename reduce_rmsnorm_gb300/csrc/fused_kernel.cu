@@ -162,9 +162,11 @@ __device__ __forceinline__ uint32_t sm_id() {
 }
 
 // Wait for the phase of the given parity of *bar to complete. Bounded: gives
-// up after kWaitLimitNs or kWaitLimitPolls polls, then sets *abort and the
-// device error word. Returns false at once while *abort is set.
-__device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned code) {
+// up after limit_ns (kWaitLimitNs in the kernels) or kWaitLimitPolls polls,
+// then sets *abort and the device error word. Returns false at once while
+// *abort is set.
+__device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned code,
+                           unsigned long long limit_ns = kWaitLimitNs) {
   if (*abort) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
@@ -172,7 +174,7 @@ __device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort, 
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0u) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) break;
+      if (global_timer_ns() - t0 > limit_ns) break;
     }
   }
   *abort = 1;
@@ -417,6 +419,21 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   }
 }
 
+// Diagnostic: one CTA waits, with the kernels' bounded wait, on an mbarrier
+// phase that nothing completes (one pending arrival that never comes). The
+// wait gives up after limit_ns and reports through the device error word.
+__global__ void wait_timeout_probe(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_phase(&bar, 0u, &abort_flag, 1u, limit_ns);
+}
+
 // ------------------------------------------------------------------ host side
 
 constexpr int kMaxDevices = 64;
@@ -578,6 +595,11 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
     return TW_ERR_CUDA;
   }
   return TW_OK;
+}
+
+int launch_wait_probe(long long limit_ns, cudaStream_t stream) {
+  wait_timeout_probe<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(limit_ns));
+  return cudaGetLastError() == cudaSuccess ? TW_OK : TW_ERR_CUDA;
 }
 
 int read_device_error(int reset, int* code) {

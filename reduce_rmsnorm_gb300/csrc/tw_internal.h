@@ -43,6 +43,9 @@ int launch_reduce(const void* const* partials, int n, int64_t rows, int64_t hidd
 int launch_add_rmsnorm(const void* sum, void* residual, const void* gamma, float eps, int64_t rows,
                        int64_t hidden, void* out, cudaStream_t stream);
 
+// Diagnostic kernel: a bounded wait on an mbarrier nothing completes.
+int launch_wait_probe(long long limit_ns, cudaStream_t stream);
+
 // Read (and optionally clear) the device-side error word of the current device.
 int read_device_error(int reset, int* code);
 

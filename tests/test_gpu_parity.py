@@ -55,6 +55,7 @@ SMALL = [
     (9, 2048, 2, 0.05, 0.0),       # exactly one chunk
     (33, 16384, 8, 0.01, 0.01),    # 405B hidden size with outliers
     (2, 32768, 2, 0.02, 0.0),      # hidden size at its maximum (16 chunks)
+    (3, 32768, 16, 0.02, 0.0),     # both maxima: 16 partials of 32768
     (300, 1024, 5, 0.02, 0.0),     # more rows than SMs
     (157, 8200, 4, 0.03, 0.0),     # ragged rows and chunks
 ]
@@ -287,3 +288,27 @@ def test_full_gpu_one_cta_per_sm():
     tw.tw_fused_debug_smid(P, R, G, EPS, out, smid)
     torch.cuda.synchronize()
     assert len(set(smid.cpu().tolist())) == sms
+
+
+def test_offsets_beyond_4gib_sampled_rows():
+    """T*H*2 > 2^32 bytes per tensor (T=70000, H=32768, N=1): 64-bit row
+    offsets. Inputs are 8 seeded rows tiled over the batch on the device; the
+    first, last and a spread of rows are checked against the oracle."""
+    T, H, N = 70000, 32768, 1
+    base_p, base_r, g = synth.make_inputs(8, H, N, 0.05, seed=70)
+    idx = torch.arange(T) % 8
+    dev = torch.device("cuda")
+    P = base_p.to(dev)[:, idx.to(dev)].contiguous()
+    R = base_r.to(dev)[idx.to(dev)].contiguous()
+    G = g.to(dev)
+    out = torch.empty_like(R)
+    torch.cuda.synchronize()
+    assert R.numel() * 2 > 2 ** 32
+    tw.tw_fused_reduce_residual_rmsnorm(P, R, G, EPS, out)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 7, 8, 32767, 32768, 65535, 65536, 65537, 69990, 69999])
+    sel = torch.from_numpy(rows)
+    check_rows(base_p[:, sel % 8], base_r[sel % 8], g, EPS, R[sel.to(dev)].cpu(),
+               out[sel.to(dev)].cpu())
+    del P, R, out
+    torch.cuda.empty_cache()
