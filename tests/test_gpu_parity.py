@@ -229,6 +229,11 @@ def test_split_configs_bitwise(T):
     sa.synchronize()
     assert_same(ref[0], R)
     assert_same(ref[1], out)
+    rng = np.random.Generator(np.random.PCG64(T))
+    rows = np.unique(np.concatenate([[0, prefix - 1, prefix, T - 1],
+                                     rng.choice(T, 64, replace=False)]))
+    rows = rows[(rows >= 0) & (rows < T)]
+    check_rows(p, r, g, EPS, R, out, rows=rows)
 
 
 @pytest.mark.parametrize("prefix", [0, 1, 2368, 4863, 4864])
