@@ -317,3 +317,34 @@ def test_offsets_beyond_4gib_sampled_rows():
                out[sel.to(dev)].cpu())
     del P, R, out
     torch.cuda.empty_cache()
+
+
+def test_split_runner_captured_in_cuda_graph():
+    """tw_run_split captured into a CUDA graph (fork and join become graph
+    edges) replays to bitwise the same result as the eager unsplit call."""
+    T = 4096
+    C = math.ceil(T / 128) * 8
+    prefix = tw.tw_wave_split(T, C, 148)[0]
+    assert 0 < prefix < T
+    p, r, g = synth.make_inputs(T, 8192, 8, 0.02, seed=44)
+    ref = run(p, r, g)
+    P, R, G = to_gpu(p, r, g)
+    R0 = R.clone()
+    out = torch.empty_like(R)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    call = tw.SplitCall(P, R, G, EPS, out, sa, sb)
+    with torch.cuda.stream(sa):
+        call(prefix)                      # eager first: attributes and events exist
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=sa):
+        call(prefix)
+    for _ in range(2):
+        R.copy_(R0)
+        out.zero_()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_same(ref[0], R)
+        assert_same(ref[1], out)
