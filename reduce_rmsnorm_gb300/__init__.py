@@ -176,18 +176,26 @@ def tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=No
     _check(st, "tw_fused_debug_smid")
 
 
+_default_opts = None
+
+
+def _opts_cached(offsets, min_split_tokens):
+    """Split options as a ctypes struct; the pages' defaults are built once."""
+    global _default_opts
+    if offsets is DEFAULT_OFFSETS and min_split_tokens == DEFAULT_MIN_SPLIT_TOKENS:
+        if _default_opts is None:
+            _default_opts = _opts(offsets, min_split_tokens)
+        return _default_opts
+    return _opts(offsets, min_split_tokens)
+
+
 def tw_wave_split(num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS,
                   min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
     """(prefix_tokens, suffix_tokens) of the wave-aware split.
 
     offsets=None means every integer offset 0 .. half-1.
     """
-    if offsets is None:
-        opts = _SplitOpts(None, 0, int(min_split_tokens))
-        keep = None
-    else:
-        keep = (ctypes.c_int * max(len(offsets), 1))(*[int(o) for o in offsets])
-        opts = _SplitOpts(keep, len(offsets), int(min_split_tokens))
+    opts, keep = _opts_cached(offsets, min_split_tokens)
     p, s = _i64(), _i64()
     st = lib().tw_wave_split(int(num_tokens), int(ctas_unsplit), int(num_sms), ctypes.byref(opts),
                              ctypes.byref(p), ctypes.byref(s))

@@ -42,6 +42,7 @@ struct NormParams {
   uint4* residual;
   const uint4* gamma;
   uint4* out;
+  long long rows;
   int vec_per_row;
   float eps;
   float hidden;
@@ -92,49 +93,54 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const __grid_con
   }
 }
 
-// One CTA per token row; thread t owns vectors t, t + 256, ... (KMAX of them).
+// One CTA per token row at a time (rows stride over the grid); thread t owns
+// vectors t, t + 256, ... (KMAX of them).
 template <int KMAX>
 __global__ void __launch_bounds__(kNormThreads) add_rmsnorm_kernel(const __grid_constant__ NormParams p) {
-  __shared__ float warp_ss[kNormThreads / 32];
+  __shared__ float warp_ss[2][kNormThreads / 32];
   const int t = threadIdx.x;
-  const long long row = blockIdx.x;
   const int vpr = p.vec_per_row;
-  const uint4* s_row = p.sum + row * vpr;
-  uint4* r_row = p.residual + row * vpr;
-  float x[KMAX][8];
-  float ss = 0.0f;
+  int buf = 0;
+  for (long long row = blockIdx.x; row < p.rows; row += gridDim.x, buf ^= 1) {
+    const uint4* s_row = p.sum + row * vpr;
+    uint4* r_row = p.residual + row * vpr;
+    float x[KMAX][8];
+    float ss = 0.0f;
 #pragma unroll
-  for (int k = 0; k < KMAX; ++k) {
-    const int v = k * kNormThreads + t;
-    if (v < vpr) {
-      float a[8];
-      unpack(__ldcs(s_row + v), a);
-      accumulate(__ldcs(r_row + v), a);
-      const uint4 stored = pack8(a);
-      r_row[v] = stored;
-      unpack(stored, x[k]);  // the norm reads the stored bf16 residual
+    for (int k = 0; k < KMAX; ++k) {
+      const int v = k * kNormThreads + t;
+      if (v < vpr) {
+        float a[8];
+        unpack(__ldcs(s_row + v), a);
+        accumulate(__ldcs(r_row + v), a);
+        const uint4 stored = pack8(a);
+        r_row[v] = stored;
+        unpack(stored, x[k]);  // the norm reads the stored bf16 residual
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(x[k][i], x[k][i], ss);
+        for (int i = 0; i < 8; ++i) ss = fmaf(x[k][i], x[k][i], ss);
+      }
     }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((t & 31) == 0) warp_ss[t >> 5] = ss;
-  __syncthreads();
-  float total = 0.0f;
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    // two buffers: a thread can only write buffer b again after every thread
+    // has passed the next row's barrier, i.e. has finished reading buffer b
+    if ((t & 31) == 0) warp_ss[buf][t >> 5] = ss;
+    __syncthreads();
+    float total = 0.0f;
 #pragma unroll
-  for (int w = 0; w < kNormThreads / 32; ++w) total += warp_ss[w];
-  const float rs = rsqrtf(total / p.hidden + p.eps);
-  uint4* o_row = p.out + row * vpr;
+    for (int w = 0; w < kNormThreads / 32; ++w) total += warp_ss[buf][w];
+    const float rs = rsqrtf(total / p.hidden + p.eps);
+    uint4* o_row = p.out + row * vpr;
 #pragma unroll
-  for (int k = 0; k < KMAX; ++k) {
-    const int v = k * kNormThreads + t;
-    if (v < vpr) {
-      float g[8], y[8];
-      unpack(__ldg(p.gamma + v), g);
+    for (int k = 0; k < KMAX; ++k) {
+      const int v = k * kNormThreads + t;
+      if (v < vpr) {
+        float g[8], y[8];
+        unpack(__ldg(p.gamma + v), g);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) y[i] = (x[k][i] * rs) * g[i];
-      o_row[v] = pack8(y);
+        for (int i = 0; i < 8; ++i) y[i] = (x[k][i] * rs) * g[i];
+        o_row[v] = pack8(y);
+      }
     }
   }
 }
@@ -185,6 +191,7 @@ int launch_add_rmsnorm(const void* sum, void* residual, const void* gamma, float
   p.residual = static_cast<uint4*>(residual);
   p.gamma = static_cast<const uint4*>(gamma);
   p.out = static_cast<uint4*>(out);
+  p.rows = rows;
   p.vec_per_row = static_cast<int>(hidden / 8);
   p.eps = eps;
   p.hidden = static_cast<float>(hidden);
@@ -192,7 +199,12 @@ int launch_add_rmsnorm(const void* sum, void* residual, const void* gamma, float
   int k = 0;
   while ((1 << k) < slots) ++k;
   if (k > 4) return TW_ERR_UNSUPPORTED;  // H <= TW_MAX_HIDDEN keeps k <= 4
-  kNorm[k]<<<static_cast<unsigned>(rows), kNormThreads, 0, stream>>>(p);
+  const int sms = sm_count();
+  if (sms <= 0) return TW_ERR_CUDA;
+  // one row per CTA up to 16 resident CTAs per SM; larger batches loop
+  const long long cap = static_cast<long long>(sms) * 16;
+  const long long grid = rows < cap ? rows : cap;
+  kNorm[k]<<<static_cast<unsigned>(grid), kNormThreads, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? TW_OK : TW_ERR_CUDA;
 }
 

@@ -43,7 +43,8 @@ def _check_unfused(p, r, g, S, R, Y):
 
 
 @pytest.mark.parametrize("T,H,N", [(1, 8, 1), (5, 4104, 3), (64, 8192, 8), (33, 16384, 8),
-                                   (3, 32768, 2), (200, 4096, 16)])
+                                   (3, 32768, 2), (200, 4096, 16),
+                                   (5000, 1024, 4)])   # more rows than the capped grid
 def test_unfused_parity(T, H, N):
     p, r, g = synth.make_inputs(T, H, N, 0.02, seed=T + N)
     P, R, G = to_gpu(p, r, g)
