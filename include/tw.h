@@ -29,6 +29,13 @@
 extern "C" {
 #endif
 
+/* Entry points are the library's only exported symbols. */
+#if defined(__GNUC__)
+#define TW_API __attribute__((visibility("default")))
+#else
+#define TW_API
+#endif
+
 struct CUstream_st;
 typedef struct CUstream_st* tw_stream_t; /* == cudaStream_t */
 struct CUevent_st;
@@ -90,7 +97,7 @@ typedef enum {
  * TW_ERR_ALIGN (H % 8 or any pointer not 16-byte aligned), TW_ERR_UNSUPPORTED
  * (H > TW_MAX_HIDDEN), TW_ERR_CUDA (device query or launch failure).
  */
-int tw_fused_reduce_residual_rmsnorm(const void* const* partials, int N, void* residual,
+TW_API int tw_fused_reduce_residual_rmsnorm(const void* const* partials, int N, void* residual,
                                      const void* gamma, float eps, int64_t T, int64_t H,
                                      void* out, tw_stream_t stream, int sm_budget);
 
@@ -137,7 +144,7 @@ typedef struct {
  * Errors: TW_ERR_INVALID_ARG (T < 0, C < 0, S <= 0, null output pointer,
  * n_offsets < 0, offsets NULL with n_offsets > 0, a negative offset).
  */
-int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_sms, const tw_split_opts* opts,
+TW_API int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_sms, const tw_split_opts* opts,
                   int64_t* prefix_tokens, int64_t* suffix_tokens);
 
 /*
@@ -157,7 +164,7 @@ int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_sms, const t
  * 0, a matching entry whose prefix is outside [0, num_tokens], or any error
  * of tw_wave_split).
  */
-int tw_split_lookup(const int64_t* table_tokens, const int64_t* table_prefix, int n_entries,
+TW_API int tw_split_lookup(const int64_t* table_tokens, const int64_t* table_prefix, int n_entries,
                     int64_t num_tokens, int64_t ctas_unsplit, int num_sms,
                     const tw_split_opts* opts, int64_t* prefix_tokens, int64_t* suffix_tokens);
 
@@ -182,7 +189,7 @@ int tw_split_lookup(const int64_t* table_tokens, const int64_t* table_prefix, in
  *
  * Arguments as for the fused call, plus prefix_tokens in [0, T].
  */
-int tw_run_split(int64_t prefix_tokens, const void* const* partials, int N, void* residual,
+TW_API int tw_run_split(int64_t prefix_tokens, const void* const* partials, int N, void* residual,
                  const void* gamma, float eps, int64_t T, int64_t H, void* out,
                  tw_stream_t stream_a, tw_stream_t stream_b, int sm_budget);
 
@@ -203,13 +210,13 @@ int tw_run_split(int64_t prefix_tokens, const void* const* partials, int N, void
  * Arguments and errors as for tw_run_split; events are cudaEvent_t handles
  * owned by the caller.
  */
-int tw_run_split_after(int64_t prefix_tokens, const void* const* partials, int N, void* residual,
+TW_API int tw_run_split_after(int64_t prefix_tokens, const void* const* partials, int N, void* residual,
                        const void* gamma, float eps, int64_t T, int64_t H, void* out,
                        tw_stream_t stream, tw_event_t prefix_ready, tw_event_t suffix_ready,
                        int sm_budget);
 
 /* Text of a tw_status value (static storage; never NULL). */
-const char* tw_strerror(int status);
+TW_API const char* tw_strerror(int status);
 
 /*
  * tw_launch_shape -- the launch the fused call would make on the current
@@ -217,7 +224,7 @@ const char* tw_strerror(int status);
  * bytes and pipeline stages. Any output pointer may be NULL. Queries device
  * attributes (TW_ERR_CUDA without a GPU). Validation as for the fused call.
  */
-int tw_launch_shape(int64_t T, int64_t H, int N, int sm_budget, int* grid, int* threads,
+TW_API int tw_launch_shape(int64_t T, int64_t H, int N, int sm_budget, int* grid, int* threads,
                     int* smem_bytes, int* stages);
 
 /*
@@ -228,7 +235,7 @@ int tw_launch_shape(int64_t T, int64_t H, int N, int sm_budget, int* grid, int* 
  * for staged data; bit 1 the producer gave up waiting for a free stage; bit 2
  * a final drain of in-flight copies gave up.
  */
-int tw_device_status(int reset, int* code);
+TW_API int tw_device_status(int reset, int* code);
 
 /*
  * tw_debug_wait_timeout -- a diagnostic of the kernels' bounded waits: one
@@ -238,7 +245,7 @@ int tw_device_status(int reset, int* code);
  * tw_device_status then reports. The GPU stays usable. For testing the
  * failure path without faulting or hanging a GPU.
  */
-int tw_debug_wait_timeout(int64_t limit_ns, tw_stream_t stream);
+TW_API int tw_debug_wait_timeout(int64_t limit_ns, tw_stream_t stream);
 
 /*
  * tw_fused_debug_smid -- the fused call, additionally writing the %smid of
@@ -246,7 +253,7 @@ int tw_debug_wait_timeout(int64_t limit_ns, tw_stream_t stream);
  * grid's length, see tw_launch_shape). For checking that an sm_budget of k
  * occupies at most k SMs.
  */
-int tw_fused_debug_smid(const void* const* partials, int N, void* residual, const void* gamma,
+TW_API int tw_fused_debug_smid(const void* const* partials, int N, void* residual, const void* gamma,
                         float eps, int64_t T, int64_t H, void* out, tw_stream_t stream,
                         int sm_budget, int* smid_out);
 
@@ -265,7 +272,7 @@ int tw_fused_debug_smid(const void* const* partials, int N, void* residual, cons
  *   Other arguments and errors as for the fused call (N 1..16, H % 8 == 0,
  *   16-byte aligned pointers, T == 0 a no-op).
  */
-int tw_reduce_partials(const void* const* partials, int N, int64_t T, int64_t H, void* sum_out,
+TW_API int tw_reduce_partials(const void* const* partials, int N, int64_t T, int64_t H, void* sum_out,
                        tw_stream_t stream);
 
 /*
@@ -279,7 +286,7 @@ int tw_reduce_partials(const void* const* partials, int N, int64_t T, int64_t H,
  *   residual   device bf16 [T, H], in/out; must not overlap sum, out or gamma.
  *   Other arguments and errors as for the fused call.
  */
-int tw_add_rmsnorm(const void* sum, void* residual, const void* gamma, float eps, int64_t T,
+TW_API int tw_add_rmsnorm(const void* sum, void* residual, const void* gamma, float eps, int64_t T,
                    int64_t H, void* out, tw_stream_t stream);
 
 #ifdef __cplusplus

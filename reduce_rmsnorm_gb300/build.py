@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libtw.so")
 
 SOURCES = ["fused_kernel.cu", "unfused_kernels.cu", "abi.cpp", "planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
               "-I", INCLUDE, "-I", CSRC] + ARCH
 
 

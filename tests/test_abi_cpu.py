@@ -26,7 +26,7 @@ def L():
 
 def _declared_symbols():
     text = open(os.path.join(ROOT, "include", "tw.h")).read()
-    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(tw_\w+)\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^TW_API\s+(?:int|const char\*)\s+(tw_\w+)\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -41,6 +41,17 @@ def test_library_exports_every_declared_symbol(L):
     assert set(_declared_symbols()) <= set(tw.EXPORTED) | set()
     for name in tw.EXPORTED:
         assert name in _declared_symbols(), name
+
+
+def test_library_exports_only_the_declared_entry_points(L):
+    import shutil
+    import subprocess
+    if shutil.which("nm") is None:
+        pytest.skip("needs nm")
+    out = subprocess.run(["nm", "-D", "--defined-only", tw.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    names = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert names == set(_declared_symbols()), sorted(names ^ set(_declared_symbols()))
 
 
 def test_strerror(L):
