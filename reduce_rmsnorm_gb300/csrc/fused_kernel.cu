@@ -261,14 +261,17 @@ __device__ __forceinline__ void reduce_vector(uint32_t src, uint32_t cbytes, int
   }
 }
 
-// KMAX: slots of a row held in registers (ceil(H/8 / 256) rounded up to a
-//       power of two, >= VPT).
-// VPT:  slots per chunk (1: 4 KiB copies; 2: 8 KiB copies).
-// NT:   compile-time partial count, or 0 for any N.
+// KMAX:  slots of a row held in registers (ceil(H/8 / 256) rounded up to a
+//        power of two, >= VPT).
+// VPT:   slots per chunk (1: 4 KiB copies; 2: 8 KiB copies).
+// NT:    compile-time partial count, or 0 for any N.
+// EXACT: H/8 == KMAX * 256 (H = 4096, 8192, 16384, 32768 with 8 KiB chunks):
+//        every chunk is full and the chunk count is a constant, so the
+//        ragged-edge checks compile away (~5% per SM under an SM budget).
 // Thread t of the consumers owns vectors t, t + 256, t + 512, ... of every row
 // (slot j = vector j * 256 + t) whatever VPT is, so the per-row arithmetic,
 // including the order of the sum of squares, depends only on H.
-template <int KMAX, int VPT, int NT>
+template <int KMAX, int VPT, int NT, bool EXACT>
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -286,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   const long long row0 = static_cast<long long>(blockIdx.x) * p.rows / grid;
   const long long row1 = static_cast<long long>(blockIdx.x + 1) * p.rows / grid;
   const int n = NT > 0 ? NT : p.n_partials;
-  const int vpr = p.vec_per_row;
-  const int chunks = p.chunks;
+  const int vpr = EXACT ? KMAX * kSlotVec : p.vec_per_row;
+  const int chunks = EXACT ? KMAX / VPT : p.chunks;
   const int stages = p.stages;
   const uint32_t stage_bytes = static_cast<uint32_t>(n + 1) * kChunkBytes;
 
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     for (long long it = 0; it < items; ++it) {
       int ok = 1;
       const int v0 = chunk * kChunkVec;
-      const int nvec = min(kChunkVec, vpr - v0);
+      const int nvec = EXACT ? kChunkVec : min(kChunkVec, vpr - v0);
       const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
       if (lane == 0) {
         if (!first_pass) ok = wait_phase(&empty_bar[s], round_parity ^ 1u, abort, 2u);
@@ -360,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       const int v = j * kSlotVec + t;
-      g_reg[j] = v < vpr ? __ldg(p.gamma + v) : make_uint4(0, 0, 0, 0);
+      g_reg[j] = (EXACT || v < vpr) ? __ldg(p.gamma + v) : make_uint4(0, 0, 0, 0);
     }
   }
   int s = 0;
@@ -377,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
           const int j = c * VPT + u;
-          if (j * kSlotVec + t < vpr) reduce_vector<NT>(stage + u * kSlotBytes, kChunkBytes, n, z[j]);
+          if (EXACT || j * kSlotVec + t < vpr)
+            reduce_vector<NT>(stage + u * kSlotBytes, kChunkBytes, n, z[j]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -385,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
         for (int u = 0; u < VPT; ++u) {
           const int j = c * VPT + u;
           const int v = j * kSlotVec + t;
-          if (v < vpr) {
+          if (EXACT || v < vpr) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss = fmaf(z[j][i], z[j][i], ss);
             res_row[v] = pack8(z[j]);
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       const int v = j * kSlotVec + t;
-      if (v < vpr) {
+      if (EXACT || v < vpr) {
         float g[8], y[8];
         if constexpr (kGammaRegs) load8(g_reg[j], g);
         else load8(__ldg(p.gamma + v), g);
@@ -442,15 +446,19 @@ constexpr int kStaticSmemReserve = 2048;  // barriers, warp sums, flag, slack
 using KernelFn = void (*)(Params);
 
 // Kernel instances. VPT = 2 (8 KiB copies) serves N <= 8 with a compile-time
-// N for 2, 4 and 8; VPT = 1 (4 KiB copies) serves N = 9..16, whose stages
-// would not fit three deep at 8 KiB.
-#define TW_NROW(K) {fused_kernel<K, 2, 0>, fused_kernel<K, 2, 2>, fused_kernel<K, 2, 4>, \
-                    fused_kernel<K, 2, 8>}
-const KernelFn kVpt2[4][4] = {TW_NROW(2), TW_NROW(4), TW_NROW(8), TW_NROW(16)};
+// N for 2, 4 and 8, each in a general and an EXACT (whole-chunk rows) form;
+// VPT = 1 (4 KiB copies) serves N = 9..16, whose stages would not fit three
+// deep at 8 KiB.
+#define TW_NROW(K, E) {fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 2, E>, \
+                       fused_kernel<K, 2, 4, E>, fused_kernel<K, 2, 8, E>}
+const KernelFn kVpt2[2][4][4] = {
+    {TW_NROW(2, false), TW_NROW(4, false), TW_NROW(8, false), TW_NROW(16, false)},
+    {TW_NROW(2, true), TW_NROW(4, true), TW_NROW(8, true), TW_NROW(16, true)}};
 #undef TW_NROW
-const KernelFn kVpt1[5] = {fused_kernel<1, 1, 0>, fused_kernel<2, 1, 0>, fused_kernel<4, 1, 0>,
-                           fused_kernel<8, 1, 0>, fused_kernel<16, 1, 0>};
-constexpr int kNumKernels = 16 + 5;
+const KernelFn kVpt1[5] = {fused_kernel<1, 1, 0, false>, fused_kernel<2, 1, 0, false>,
+                           fused_kernel<4, 1, 0, false>, fused_kernel<8, 1, 0, false>,
+                           fused_kernel<16, 1, 0, false>};
+constexpr int kNumKernels = 32 + 5;
 
 // Per-device attributes, queried once; the launch path reads them without a
 // lock once `ready` is set (the flags live in static storage, so they start
@@ -483,10 +491,11 @@ void select_kernel(int vpr, int n, int* index, KernelFn* fn, int* kmax) {
   *kmax = 1 << k;
   if (vpt == 2) {
     const int ki = k - 1, ni = partials_index(n);  // KMAX 2..16
-    *index = ki * 4 + ni;
-    *fn = kVpt2[ki][ni];
+    const int exact = vpr == (1 << k) * kSlotVec ? 1 : 0;
+    *index = exact * 16 + ki * 4 + ni;
+    *fn = kVpt2[exact][ki][ni];
   } else {
-    *index = 16 + k;  // KMAX 1..16
+    *index = 32 + k;  // KMAX 1..16
     *fn = kVpt1[k];
   }
 }
