@@ -105,28 +105,35 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = []
-        for line in out.splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                rows.append(dict(sm=float(f[1]), max=float(f[2]), power=float(f[3]),
-                                 hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
-            except ValueError:
-                continue
-        if not rows:
-            return None
-        reasons = set()
-        for r in rows:
-            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
-                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
-                if r[key].lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
-                "sm_max_mhz": max(r["max"] for r in rows),
-                "power_w_max": max(r["power"] for r in rows),
-                "samples": len(rows), "reasons": sorted(reasons)}
+        return parse_clock_lines(out.splitlines())
+
+
+def parse_clock_lines(lines):
+    """Summarise `nvidia-smi --query-gpu=<ClockSampler.FIELDS> --format=csv,noheader,nounits`
+    lines: median SM clock, max clock, max power, and the throttle reasons seen
+    active in any sample. None if no line parses."""
+    rows = []
+    for line in lines:
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            rows.append(dict(sm=float(f[1]), max=float(f[2]), power=float(f[3]),
+                             hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    reasons = set()
+    for r in rows:
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+            if r[key].lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+            "sm_max_mhz": max(r["max"] for r in rows),
+            "power_w_max": max(r["power"] for r in rows),
+            "samples": len(rows), "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------------------ distributed plumbing

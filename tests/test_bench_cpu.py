@@ -1,0 +1,56 @@
+"""bench.py's host-side helpers on the CPU: roofline denominator and its
+fallback, the ncu traffic record tied to the kernel source revision, the
+clock-record summary, and the split workload's CTA model."""
+
+import json
+
+import bench
+
+
+def test_peak_from_measured_file_or_fallback(tmp_path, monkeypatch):
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 1234.5}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.peak_hbm() == (1234.5, "measured")
+    (tmp_path / "MEASURED_PEAKS.json").unlink()
+    assert bench.peak_hbm() == (bench.FALLBACK_HBM_GBS, "fallback")
+
+
+def test_traffic_record_only_for_the_profiled_kernel(tmp_path, monkeypatch):
+    rec = {"kernel_sha": bench.kernel_sha(),
+           "workloads": {"w": {"dram_bytes_per_launch": 157229312}}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(path))
+    assert bench.ncu_traffic("w") == 157229312
+    assert bench.ncu_traffic("other") is None
+    rec["kernel_sha"] = "0" * 16          # the kernel changed since the capture
+    path.write_text(json.dumps(rec))
+    assert bench.ncu_traffic("w") is None
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "missing.json"))
+    assert bench.ncu_traffic("w") is None
+
+
+def test_committed_traffic_record_matches_current_kernel():
+    # the committed record must describe the committed kernel source
+    assert bench.ncu_traffic("llama70b_t1024_h8192_n8") is not None
+
+
+def test_clock_lines_summary():
+    lines = [
+        "0, 2070, 2070, 480.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2070, 2070, 510.3, 0x0, Not Active, Not Active, Not Active, Active",
+        "0, 1980, 2070, 505.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "garbage line",
+    ]
+    c = bench.parse_clock_lines(lines)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0
+    assert c["power_w_max"] == 510.3 and c["reasons"] == ["sw_power_cap"]
+    hot = ["0, 1500, 2070, 900.0, 0x40, Not Active, Active, Not Active, Not Active"]
+    assert bench.parse_clock_lines(hot)["reasons"] == ["hw_thermal_slowdown"]
+    assert bench.parse_clock_lines([]) is None
+
+
+def test_cta_model_of_the_split_workload():
+    # ceil(T/128) * (H/128) / 8: the configs' 64 / 128 / 256 / 512 CTAs
+    assert [bench.ctas_unsplit(T, 8192) for T in (1024, 2048, 4096, 8192)] == [64, 128, 256, 512]
+    assert bench.ctas_unsplit(4864, 8192) == 304
