@@ -30,11 +30,6 @@ def test_traffic_record_only_for_the_profiled_kernel(tmp_path, monkeypatch):
     assert bench.ncu_traffic("w") is None
 
 
-def test_committed_traffic_record_matches_current_kernel():
-    # the committed record must describe the committed kernel source
-    assert bench.ncu_traffic("llama70b_t1024_h8192_n8") is not None
-
-
 def test_clock_lines_summary():
     lines = [
         "0, 2070, 2070, 480.1, 0x0, Not Active, Not Active, Not Active, Not Active",
