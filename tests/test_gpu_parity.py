@@ -348,3 +348,26 @@ def test_split_runner_captured_in_cuda_graph():
         torch.cuda.synchronize()
         assert_same(ref[0], R)
         assert_same(ref[1], out)
+
+
+def _random_shapes(count, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shapes = []
+    while len(shapes) < count:
+        H = 8 * int(rng.integers(1, 4097))
+        N = int(rng.integers(1, 17))
+        T = int(rng.integers(1, 400))
+        if T * H * (N + 1) > 3_000_000:     # keep the oracle to seconds
+            continue
+        budget = int(rng.choice([0, 0, 1, 3, 7, 33]))
+        shapes.append((T, H, N, budget))
+    return shapes
+
+
+@pytest.mark.parametrize("T,H,N,budget", _random_shapes(24, 2026))
+def test_parity_random_shapes(T, H, N, budget):
+    """Seeded random shapes: any hidden size that is a multiple of 8 (ragged
+    chunks), 1..16 partials, ragged row counts, SM budgets; every row checked."""
+    p, r, g = synth.make_inputs(T, H, N, 0.03, seed=T + H + N)
+    R, out = run(p, r, g, sm_budget=budget)
+    check_rows(p, r, g, EPS, R, out)
