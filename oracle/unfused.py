@@ -3,11 +3,11 @@ standalone residual-add + RMSNorm that reads it back.
 
 TEST INFRASTRUCTURE (see the package docstring).
 
-This is the one-GPU analogue of the pipeline the pages compare against:
-"AllReduce, then RMSNorm" ([W] "Fix two": vLLM runs RMSNorm after AllReduce,
-and standard RMSNorm reads the tensor twice and writes it once; [G] "The
-Standard RMSNorm Memory Round-Trip": the reduced tensor is written to HBM and
-read back by a separate kernel). Its arithmetic differs from the fused step
+This is the one-GPU analogue of the pipeline the pages compare against, an
+all-reduce followed by a separate RMSNorm ([W] "Fix two": the serving engine
+normalises after the all-reduce, and a standalone RMSNorm reads its input
+twice and writes once; [G] "The Standard RMSNorm Memory Round-Trip": the
+reduced tensor goes to HBM and a second kernel reads it back). Its arithmetic differs from the fused step
 only by two extra bf16 roundings that the HBM round trip forces:
 
     S   = bf16( ((P_0 + P_1) + ...) + P_{N-1} )      fp32 adds, rank order

@@ -1,5 +1,6 @@
-// Unfused baseline for sm_103a: the one-GPU analogue of "AllReduce, then
-// RMSNorm" that the fused step replaces.
+// Unfused baseline for sm_103a: the one-GPU analogue of the pipeline the fused
+// step replaces, an all-reduce that writes its result to memory followed by a
+// separate RMSNorm kernel.
 //
 // [W] = "TokenWeave: Why Hiding Tensor-Parallel Communication Needs Wave
 // Arithmetic, Not Finer Tiles", "Fix two": vLLM runs RMSNorm after the
