@@ -7,8 +7,9 @@ This is the one-GPU analogue of the pipeline the pages compare against, an
 all-reduce followed by a separate RMSNorm ([W] "Fix two": the serving engine
 normalises after the all-reduce, and a standalone RMSNorm reads its input
 twice and writes once; [G] "The Standard RMSNorm Memory Round-Trip": the
-reduced tensor goes to HBM and a second kernel reads it back). Its arithmetic differs from the fused step
-only by two extra bf16 roundings that the HBM round trip forces:
+reduced tensor goes to HBM and a second kernel reads it back). Its arithmetic
+differs from the fused step only by two extra bf16 roundings that the HBM
+round trip forces:
 
     S   = bf16( ((P_0 + P_1) + ...) + P_{N-1} )      fp32 adds, rank order
     x   = fp32(S) + fp32(R)                           fp32 add
