@@ -3,7 +3,9 @@
 Tolerances (floating point; the pages fix no precision beyond bf16 storage):
   * updated residual: bit-exact to the oracle's fp32 rank-order emulation
     (only IEEE additions are involved, so no rounding freedom), and within
-    1 bf16 ulp of the exact fp64 sum.
+    1 bf16 ulp of the exact fp64 sum plus the fp32 summation bound
+    N * 2^-24 * (sum_r |P_r| + |R|); the bound matters only where the terms
+    cancel to a result much smaller than themselves.
   * output Y: |Y - y64| <= 2 * ulp_bf16(y64) + delta, with
     delta = r * |gamma_j| * N * 2^-24 * (sum_r |P_r| + |R|), the fp32
     summation error bound of the N additions carried through the scale
@@ -42,12 +44,13 @@ def check_rows(partials_cpu, residual_cpu, gamma_cpu, eps, res_gpu, out_gpu, row
     emu = fused.residual_fp32_rank_order(pb, rb)
     mism = np.count_nonzero(emu != res_bits)
     assert mism == 0, "updated residual differs from fp32 rank-order emulation in %d places" % mism
-    r_dec = bf16.decode(res_bits)
-    assert np.all(np.abs(r_dec - z64) <= bf16.ulp(z64)), "residual beyond 1 ulp of exact"
-    # output: 2 ulp + fp32 summation floor
     absum = np.abs(bf16.decode(rb))
     for r in range(n):
         absum = absum + np.abs(bf16.decode(pb[r]))
+    r_dec = bf16.decode(res_bits)
+    assert np.all(np.abs(r_dec - z64) <= bf16.ulp(z64) + n * 2.0 ** -24 * absum), \
+        "residual beyond 1 ulp of exact plus the fp32 summation bound"
+    # output: 2 ulp + fp32 summation floor
     ms = np.mean(z64 * z64, axis=1, keepdims=True)
     rscale = 1.0 / np.sqrt(ms + eps)
     g64 = np.abs(bf16.decode(gb))[None, :]

@@ -122,6 +122,29 @@ def test_zero_and_constant_rows():
     assert torch.allclose(o[2], want.to(torch.bfloat16).float(), rtol=2 ** -7, atol=0)
 
 
+def test_subnormal_inputs_are_not_flushed():
+    """bf16 subnormals (|x| < 2^-126) in partials and residual: the fp32 sums
+    must keep them (no flush to zero), so the updated residual stays bit-exact
+    to the IEEE fp32 emulation; rows of only subnormals normalise to tiny
+    outputs within tolerance."""
+    T, H, N = 8, 2048, 4
+    rng = np.random.Generator(np.random.PCG64(126))
+    mags = np.ldexp(1.0, rng.integers(-133, -126, size=(N + 1, T, H)))
+    vals = mags * rng.choice([-1.0, 1.0], size=(N + 1, T, H)) * rng.integers(1, 128, size=(N + 1, T, H))
+    vals[:, :4] = np.where(rng.random((N + 1, 4, H)) < 0.5, vals[:, :4],
+                           rng.standard_normal((N + 1, 4, H)) * 1e-3)   # mixed rows
+    from oracle import bf16 as obf16
+    bits = obf16.encode_rne(vals)
+    as_bf16 = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    p, r = as_bf16[:N].contiguous(), as_bf16[N].contiguous()
+    g = synth.make_inputs(1, H, 1, 0.02, seed=5)[2]
+    R, out = run(p, r, g)
+    check_rows(p, r, g, EPS, R, out)
+    b = synth.bits(R.cpu())
+    subnormal = ((b & 0x7F80) == 0) & ((b & 0x7F) != 0)
+    assert subnormal.any()   # subnormal results were produced
+
+
 def test_small_integer_partials_exact():
     T, H, N = 4, 1024, 8
     gen = torch.Generator().manual_seed(3)

@@ -344,3 +344,37 @@ def test_golden_files_cite_sources():
     for name in ("planner_pins.txt", "bf16_bits.txt", "bf16_rne.txt", "rmsnorm_closed_forms.txt"):
         text = open(os.path.join(GOLDEN, name)).read()
         assert re.search(r"\[(W|G)\]|IEEE", text), name
+
+
+def test_fp64_oracle_against_50_digit_decimal_reference():
+    """The fp64 oracle against exact decimal arithmetic (50 digits): the sum of
+    bf16 values is exact in Decimal, the mean square and square root are
+    correctly rounded at 50 digits. Rows include heavy cancellation and
+    outliers. The oracle must agree to 1e-12 relative (it is the reference the
+    GPU is held to within 2 bf16 ulps, ~8e-3)."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    rng = np.random.Generator(np.random.PCG64(50))
+    n, t, h = 4, 6, 96
+    p = rng.standard_normal((n, t, h)) * 0.02
+    p[:, 2] *= 1e4                       # large partials ...
+    p[3, 2] = -p[:3, 2].sum(axis=0)      # ... that nearly cancel
+    r = rng.standard_normal((t, h))
+    r[4, ::7] *= 300.0                   # outliers
+    pb, rb = bf16.encode_rne(p), bf16.encode_rne(r)
+    gb = bf16.encode_rne(rng.uniform(0.5, 1.5, size=h))
+    eps = 1e-5
+    z64, y64 = fused.reduce_residual_rmsnorm(pb, rb, gb, eps)
+    P, R, G = bf16.decode(pb), bf16.decode(rb), bf16.decode(gb)
+    for a in range(t):
+        z = [sum((Decimal(float(P[k, a, b])) for k in range(n)), Decimal(float(R[a, b])))
+             for b in range(h)]
+        ms = sum(v * v for v in z) / h
+        scale = (ms + Decimal(eps)).sqrt()
+        for b in range(h):
+            y = z[b] / scale * Decimal(float(G[b]))
+            assert float(z[b]) == z64[a, b]
+            if y != 0:
+                assert abs(float(y) - y64[a, b]) <= 1e-12 * abs(float(y)), (a, b)
+            else:
+                assert y64[a, b] == 0
