@@ -177,12 +177,14 @@ def job_throughput(units_per_rank, elapsed_s_max, world):
 # ------------------------------------------------------------------ the GPU arm
 
 
-def make_sets(name, T_override, l2_bytes, device):
+def make_sets(name, T_override, l2_bytes, device, N_override=0):
     import torch
     import synth
     w = dict(synth.WORKLOADS[name])
     if T_override:
         w["T"] = T_override
+    if N_override:
+        w["N"] = N_override
     T, H, N = w["T"], w["H"], w["N"]
     per_set = (N + 2) * T * H * 2 + H * 2  # resident bytes of one set (inputs + output)
     nsets = max(1, math.ceil(4 * l2_bytes / per_set))
@@ -499,8 +501,9 @@ def sweep(args):
     peak, _ = peak_hbm()
     tokens = [int(t) for t in args.sweep_tokens.split(",")]
     budgets = [int(b) for b in args.sweep_budgets.split(",")]
-    for T in tokens:
-        T_, H, N, sets, per_set = make_sets("llama70b_t1024_h8192_n8", T, l2, dev)
+    partials = [int(n) for n in args.sweep_partials.split(",")]
+    for T, Nsw in [(t, n) for t in tokens for n in partials]:
+        T_, H, N, sets, per_set = make_sets("llama70b_t1024_h8192_n8", T, l2, dev, Nsw)
         bytes_call = tw.bytes_per_call(T, H, N)
         for budget in budgets:
             reps = args.sweep_reps
@@ -763,6 +766,7 @@ def main(argv=None):
     ap.add_argument("--sweep-tokens", default="512,1024,2048,4096,8192,16384")
     ap.add_argument("--sweep-budgets", default="2,4,8,16,0")
     ap.add_argument("--sweep-reps", type=int, default=50)
+    ap.add_argument("--sweep-partials", default="8", help="N values for --sweep")
     ap.add_argument("--corun", action="store_true")
     ap.add_argument("--corun-tokens", default="1024,2048,4096,8192")
     ap.add_argument("--corun-budgets", default="2,4,8,16,0")
