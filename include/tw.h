@@ -83,7 +83,9 @@ typedef enum {
  *   eps        >= 0 and finite (1e-5 for the Llama workloads).
  *   T          token rows, >= 0; T == 0 is a no-op returning TW_OK.
  *   H          hidden size, 8 .. TW_MAX_HIDDEN, a multiple of 8.
- *   out        device bf16 [T, H], written.
+ *   out        device bf16 [T, H], written. It may be exactly the buffer of
+ *              one partial (out == partials[r]) to write Y over that rank's
+ *              partial; no other overlap with an input is allowed.
  *   stream     the stream to launch on.
  *   sm_budget  0: use the whole GPU (one CTA per SM). k > 0: launch at most k
  *              CTAs, each owning one SM (it requests enough shared memory that
@@ -93,7 +95,8 @@ typedef enum {
  *              clamped. Negative is invalid.
  *
  * Errors: TW_ERR_INVALID_ARG (N, T, H <= 0, eps, sm_budget, a null pointer,
- * residual/out overlapping each other or any input, T*H too large),
+ * residual/out overlapping each other or any input other than out ==
+ * partials[r], T*H too large),
  * TW_ERR_ALIGN (H % 8 or any pointer not 16-byte aligned), TW_ERR_UNSUPPORTED
  * (H > TW_MAX_HIDDEN), TW_ERR_CUDA (device query or launch failure).
  */

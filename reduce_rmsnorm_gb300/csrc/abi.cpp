@@ -43,12 +43,16 @@ int validate(const void* const* partials, int N, void* residual, const void* gam
     if (!aligned16(partials[r])) return TW_ERR_ALIGN;
   if (!aligned16(residual) || !aligned16(gamma) || !aligned16(out)) return TW_ERR_ALIGN;
   const int64_t bytes = T * H * 2;
-  // The two written tensors may overlap nothing else (inputs may alias each other).
+  // The two written tensors may overlap nothing else (inputs may alias each
+  // other), except that out may be exactly one partial's buffer: a row's
+  // partial chunks are all staged before the row's output is written, and
+  // staging runs ahead only into later rows.
   if (overlap(residual, out, bytes)) return TW_ERR_INVALID_ARG;
   for (void* w : {residual, out}) {
     if (overlap(w, gamma, H * 2)) return TW_ERR_INVALID_ARG;
     for (int r = 0; r < N; ++r)
-      if (overlap(w, partials[r], bytes)) return TW_ERR_INVALID_ARG;
+      if (overlap(w, partials[r], bytes) && !(w == out && out == partials[r]))
+        return TW_ERR_INVALID_ARG;
   }
   for (int r = 0; r < N; ++r) a->partials[r] = partials[r];
   a->n = N;

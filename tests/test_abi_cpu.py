@@ -200,9 +200,10 @@ def test_validation_overlaps(L):
     r = BASE + (40 << 24)
     # out overlapping the residual (by one row) is rejected
     assert _fused(L, T=T, H=H, residual=r, out=r + H * 2) == tw.TW_ERR_INVALID_ARG
-    # out adjacent to the residual is fine up to the CUDA call; here check only
-    # that a written tensor overlapping a partial or gamma is rejected
+    # a written tensor partly overlapping a partial or gamma is rejected
     assert _fused(L, T=T, H=H, out=BASE + (1 << 24) + 16) == tw.TW_ERR_INVALID_ARG
+    # the residual may not alias a partial, even exactly
+    assert _fused(L, T=T, H=H, residual=BASE + (1 << 24)) == tw.TW_ERR_INVALID_ARG
     assert _fused(L, T=T, H=H, residual=BASE + (41 << 24) - 16) == tw.TW_ERR_INVALID_ARG
     # partials aliasing one another is allowed by validation (reads only):
     # the call gets past validation and fails only at the first CUDA call

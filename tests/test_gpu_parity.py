@@ -394,3 +394,23 @@ def test_parity_random_shapes(T, H, N, budget):
     p, r, g = synth.make_inputs(T, H, N, 0.03, seed=T + H + N)
     R, out = run(p, r, g, sm_budget=budget)
     check_rows(p, r, g, EPS, R, out)
+
+
+@pytest.mark.parametrize("which,budget,split", [(0, 0, False), (7, 0, False), (3, 4, False),
+                                                 (0, 0, True)])
+def test_output_written_over_a_partial(which, budget, split):
+    """out == partials[r]: Y written over one rank's partial equals the result
+    into a separate buffer, bit for bit (also under an SM budget and split)."""
+    T, H, N = 2048, 8192, 8
+    p, r, g = synth.make_inputs(T, H, N, 0.02, seed=91)
+    ref = run(p, r, g, sm_budget=budget)
+    P, R, G = to_gpu(p, r, g)
+    out = P[which]
+    if split:
+        sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+        tw.tw_run_split(T // 2 + 64, P, R, G, EPS, out, sa, sb, sm_budget=budget)
+    else:
+        tw.tw_fused_reduce_residual_rmsnorm(P, R, G, EPS, out, sm_budget=budget)
+    torch.cuda.synchronize()
+    assert_same(ref[0], R)
+    assert_same(ref[1], out)
