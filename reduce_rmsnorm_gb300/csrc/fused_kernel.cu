@@ -445,20 +445,22 @@ constexpr int kStaticSmemReserve = 2048;  // barriers, warp sums, flag, slack
 
 using KernelFn = void (*)(Params);
 
-// Kernel instances. VPT = 2 (8 KiB copies) serves N <= 8 with a compile-time
-// N for 2, 4 and 8, each in a general and an EXACT (whole-chunk rows) form;
-// VPT = 1 (4 KiB copies) serves N = 9..16, whose stages would not fit three
-// deep at 8 KiB.
-#define TW_NROW(K, E) {fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 2, E>, \
-                       fused_kernel<K, 2, 4, E>, fused_kernel<K, 2, 8, E>}
-const KernelFn kVpt2[2][4][4] = {
-    {TW_NROW(2, false), TW_NROW(4, false), TW_NROW(8, false), TW_NROW(16, false)},
-    {TW_NROW(2, true), TW_NROW(4, true), TW_NROW(8, true), TW_NROW(16, true)}};
-#undef TW_NROW
-const KernelFn kVpt1[5] = {fused_kernel<1, 1, 0, false>, fused_kernel<2, 1, 0, false>,
-                           fused_kernel<4, 1, 0, false>, fused_kernel<8, 1, 0, false>,
-                           fused_kernel<16, 1, 0, false>};
-constexpr int kNumKernels = 32 + 5;
+// Kernel instances. VPT = 2 (8 KiB copies) serves N <= 8, with a compile-time
+// N for 1, 2, 4 and 8; VPT = 1 (4 KiB copies) serves N = 9..16, whose stages
+// would not fit three deep at 8 KiB, with a compile-time N for 16. Every
+// shape exists in a general and an EXACT (whole-chunk rows) form.
+#define TW_V2(K, E) {fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 1, E>, fused_kernel<K, 2, 2, E>, \
+                     fused_kernel<K, 2, 4, E>, fused_kernel<K, 2, 8, E>}
+const KernelFn kVpt2[2][4][5] = {
+    {TW_V2(2, false), TW_V2(4, false), TW_V2(8, false), TW_V2(16, false)},
+    {TW_V2(2, true), TW_V2(4, true), TW_V2(8, true), TW_V2(16, true)}};
+#undef TW_V2
+#define TW_V1(K, E) {fused_kernel<K, 1, 0, E>, fused_kernel<K, 1, 16, E>}
+const KernelFn kVpt1[2][5][2] = {
+    {TW_V1(1, false), TW_V1(2, false), TW_V1(4, false), TW_V1(8, false), TW_V1(16, false)},
+    {TW_V1(1, true), TW_V1(2, true), TW_V1(4, true), TW_V1(8, true), TW_V1(16, true)}};
+#undef TW_V1
+constexpr int kNumKernels = 40 + 20;
 
 // Per-device attributes, queried once; the launch path reads them without a
 // lock once `ready` is set (the flags live in static storage, so they start
@@ -479,7 +481,9 @@ int log2_pow2_at_least(int x) {
   return k;
 }
 
-int partials_index(int n) { return n == 2 ? 1 : n == 4 ? 2 : n == 8 ? 3 : 0; }
+// Column of the instance tables for N (0: runtime N).
+int partials_index_vpt2(int n) { return n == 1 ? 1 : n == 2 ? 2 : n == 4 ? 3 : n == 8 ? 4 : 0; }
+int partials_index_vpt1(int n) { return n == 16 ? 1 : 0; }
 
 int vpt_for(int n) { return n <= 8 ? 2 : 1; }
 
@@ -489,14 +493,15 @@ void select_kernel(int vpr, int n, int* index, KernelFn* fn, int* kmax) {
   const int chunks = (vpr + kSlotVec * vpt - 1) / (kSlotVec * vpt);
   const int k = log2_pow2_at_least(chunks * vpt);  // KMAX = 2^k
   *kmax = 1 << k;
+  const int exact = vpr == (1 << k) * kSlotVec ? 1 : 0;
   if (vpt == 2) {
-    const int ki = k - 1, ni = partials_index(n);  // KMAX 2..16
-    const int exact = vpr == (1 << k) * kSlotVec ? 1 : 0;
-    *index = exact * 16 + ki * 4 + ni;
+    const int ki = k - 1, ni = partials_index_vpt2(n);  // KMAX 2..16
+    *index = exact * 20 + ki * 5 + ni;
     *fn = kVpt2[exact][ki][ni];
   } else {
-    *index = 32 + k;  // KMAX 1..16
-    *fn = kVpt1[k];
+    const int ni = partials_index_vpt1(n);  // KMAX 1..16
+    *index = 40 + exact * 10 + k * 2 + ni;
+    *fn = kVpt1[exact][k][ni];
   }
 }
 
