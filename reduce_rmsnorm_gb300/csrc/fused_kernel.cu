@@ -15,16 +15,19 @@
 //   * Warp-specialised: the producer warp streams each row, in chunks of 8 KiB
 //     (N <= 8) or 4 KiB of every source (N partials + residual), from HBM into
 //     a ring of shared-memory stages with 1-D TMA bulk copies (cp.async.bulk,
-//     mbarrier completion, L2 evict-first); lane r issues source r's copy, so
-//     the N + 1 copies of a stage go out in parallel (one lane issuing them in
-//     turn, or 4 KiB copies, caps an SM near 45 GB/s). Eight consumer warps
+//     mbarrier completion); lane r issues source r's copy, so the N + 1
+//     copies of a stage go out in parallel (one lane issuing them in turn, or
+//     4 KiB copies, caps an SM near 45 GB/s). Eight consumer warps
 //     read a chunk (one or two 16-byte vectors per thread per source), sum in
 //     fp32 in rank order (packed f32x2 adds), add the residual, store the
 //     updated residual, and keep z in registers.
 //   * After a row's last chunk: warp xor-shuffle sum of squares, a fixed-order
 //     combine of the 8 warp sums, rsqrtf, and Y = (z * r) * gamma stored with
-//     16-byte stores, evict-first when the output is at most half the L2. The per-row arithmetic depends only on H, so every grid
+//     16-byte stores. The per-row arithmetic depends only on H, so every grid
 //     size (SM budget), split and shard gives bitwise the same rows.
+//   * L2 policy per call: when the output fits in a quarter of the L2, the
+//     loads are evict-first and the output is stored streaming; larger calls
+//     use the normal policy for both.
 //   * Programmatic dependent launch: the CTAs set up their barriers while the
 //     previous kernel in the stream drains, then wait (griddepcontrol.wait)
 //     before touching global memory.
@@ -67,7 +70,7 @@ struct Params {
   uint4* residual;
   uint4* out;
   int* smid_out;
-  int stream_out;   // 1: evict-first stores of the output (output <= L2 / 2)
+  int l2_stream;    // 1: evict-first loads and streaming output stores (output <= L2 / 4)
   long long rows;
   int vec_per_row;  // H / 8
   int n_partials;
@@ -123,6 +126,12 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 
@@ -318,7 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     // ring; lane r < N copies partial r, lane N the residual.
     if (lane > n) return;
     const unsigned lanes = n + 1 == 32 ? 0xffffffffu : ((1u << (n + 1)) - 1u);
-    const uint64_t policy = l2_evict_first_policy();
+    // Small calls (output <= L2 / 4) load evict-first, larger ones with the
+    // normal policy. Measured on H = 4096-16384, N = 2-16: evict-first gains
+    // 0.7-4% while the output fits in a quarter of the L2 and loses 1.5-5%
+    // above it, where the inputs of a launch far exceed the L2.
+    const uint64_t policy = p.l2_stream ? l2_evict_first_policy() : l2_evict_normal_policy();
     const uint4* src_base = lane < n ? p.partials[lane] : p.residual;
     const long long items = (row1 - row0) * chunks;
     long long issued = 0;
@@ -418,14 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
         else load8(__ldg(p.gamma + v), g);
 #pragma unroll
         for (int i = 0; i < 8; ++i) y[i] = (z[j][i] * rs) * g[i];
-        // When the output is at most half the L2, store it evict-first: its
-        // lines drain during this launch rather than competing with the next
-        // launch's reads (+2-4% at T <= 4096, H = 8192). A larger output is
-        // evicted during the launch anyway, and evict-first there measured
-        // -2.7%. A kernel that reads Y right after still finds it unless L2
-        // needs the room. The residual keeps the default policy (evict-first
-        // there measured -1%).
-        if (p.stream_out) __stcs(out_row + v, pack8(y));
+        // Small calls store the output evict-first, with the loads: its lines
+        // drain during this launch rather than competing with the next
+        // launch's reads (+1-4% at output <= L2 / 4). With normal loads the
+        // store policy measured within 0.2%. A kernel that reads Y right after
+        // still finds it unless L2 needs the room. The residual keeps the
+        // default policy (evict-first there measured -1%).
+        if (p.l2_stream) __stcs(out_row + v, pack8(y));
         else out_row[v] = pack8(y);
       }
     }
@@ -581,7 +593,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
   p.residual = static_cast<uint4*>(a.residual);
   p.out = static_cast<uint4*>(a.out);
   p.smid_out = smid_out;
-  p.stream_out = a.rows * a.hidden * 2 <= static_cast<int64_t>(d->l2_bytes) / 2 ? 1 : 0;
+  p.l2_stream = a.rows * a.hidden * 2 <= static_cast<int64_t>(d->l2_bytes) / 4 ? 1 : 0;
   p.rows = a.rows;
   p.vec_per_row = static_cast<int>(a.hidden / 8);
   p.n_partials = a.n;
