@@ -313,6 +313,9 @@ def gpu_arm(args, rank, world):
     if rank == 0:
         e2e = e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb)
         cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline(args.workload, args.tokens)
+        cpu_procs = None
+        if cpu is not None:
+            cpu_procs = cpu_baseline_procs(args.workload, args.tokens, cpu.pop("t_row_s"))
         result = {
             "metric": METRIC, "value": round(value_gbs, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
@@ -341,7 +344,7 @@ def gpu_arm(args, rank, world):
                         "p10": round(step_us[len(step_us) // 10], 3),
                         "p90": round(step_us[(9 * len(step_us)) // 10], 3),
                         "n": n_dist, "note": "events around each step (separate pass)"},
-            "unfused": unfused, "cpu_baseline": cpu, "e2e": e2e,
+            "unfused": unfused, "cpu_baseline": cpu, "cpu_baseline_procs": cpu_procs, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
@@ -453,7 +456,67 @@ def cpu_baseline(workload, T_override, budget_s=10.0):
     gbs = tw.bytes_per_call(rows, H, N) / secs / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "first %d of %d token rows of %s (fp64 NumPy oracle, one process), %.1f s"
-                      % (rows, T, workload, secs)}
+                      % (rows, T, workload, secs),
+            "t_row_s": secs / rows}
+
+
+def _oracle_shard_worker(workload, T_override, rows, seed, barrier, queue):
+    """One worker of the multi-process oracle timing: builds its shard's
+    inputs, waits for the others, then times the oracle on its rows."""
+    try:
+        import synth
+        from oracle import fused
+        w = dict(synth.WORKLOADS[workload])
+        w["T"] = rows
+        p, r, g = synth.make_inputs(seed=seed, **w)
+        pb, rb, gb = synth.bits(p), synth.bits(r), synth.bits(g)
+        barrier.wait(timeout=600)
+        t0 = time.perf_counter()  # CLOCK_MONOTONIC: comparable across processes
+        fused.reduce_residual_rmsnorm(pb, rb, gb, 1e-5)
+        fused.residual_fp32_rank_order(pb, rb)
+        queue.put((t0, time.perf_counter()))
+    except Exception as e:  # reported by the parent as a missing figure
+        queue.put(("error", repr(e)))
+
+
+def cpu_baseline_procs(workload, T_override, t_row_s, budget_s=10.0):
+    """The oracle over token shards in one spawned process per host core: the
+    workload's rows (or as many as fit the budget) split into P contiguous
+    shards. Returns None if a worker fails."""
+    import multiprocessing as mp
+    import queue as queue_mod
+    import reduce_rmsnorm_gb300 as tw
+    import synth
+    w = synth.WORKLOADS[workload]
+    T = T_override or w["T"]
+    P = len(os.sched_getaffinity(0))
+    rows_total = int(max(1, min(T, P * budget_s / max(t_row_s, 1e-6))))
+    per = [rows_total // P + (1 if i < rows_total % P else 0) for i in range(P)]
+    per = [n for n in per if n > 0]
+    ctx = mp.get_context("spawn")  # the parent has a CUDA context: never fork
+    bar, q = ctx.Barrier(len(per)), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_shard_worker, args=(workload, T_override, n, i, bar, q))
+             for i, n in enumerate(per)]
+    for pr in procs:
+        pr.start()
+    spans = []
+    try:
+        for _ in procs:
+            spans.append(q.get(timeout=900))
+    except queue_mod.Empty:
+        spans.append(("error", "timeout"))
+    for pr in procs:
+        pr.join(timeout=60)
+        if pr.is_alive():
+            pr.kill()
+    if any(sp[0] == "error" for sp in spans):
+        return None
+    wall = max(e for _, e in spans) - min(s0 for s0, _ in spans)
+    return {"value": round(tw.bytes_per_call(rows_total, w["H"], w["N"]) / wall / 1e9, 4),
+            "unit": "GB/s", "cores": len(per), "kind": "oracle",
+            "sample": "%d of %d token rows of %s in %d contiguous shards, one spawned process "
+                      "per shard (fp64 NumPy oracle), %.2f s wall" % (
+                          rows_total, T, workload, len(per), wall)}
 
 
 def reference_arm(args, rank, world):
@@ -490,7 +553,10 @@ def reference_arm(args, rank, world):
 
 def sweep(args):
     """GB/s and GB/s per SM for T = 512..16384 and budgets 2/4/8/16/full
-    (H=8192, N=8); one JSON line per cell."""
+    (H=8192, N=8); one JSON line per cell. The headline figure per cell is the
+    median of per-launch CUDA events (launch latency included); b2b_us and
+    graph_us are the mean per launch over the same launches issued back to
+    back eagerly and replayed from one CUDA graph."""
     import torch
     import reduce_rmsnorm_gb300 as tw
     from reduce_rmsnorm_gb300 import build
@@ -525,7 +591,40 @@ def sweep(args):
             med = us[len(us) // 2]
             used = tw.tw_launch_shape(T, H, N, budget)["grid"]
             gbs = bytes_call / (med / 1e6) / 1e9
-            extra = {}
+            # launch-overhead context: the same launches back to back (eager,
+            # programmatic dependent launch) and replayed from one CUDA graph
+            ss = torch.cuda.Stream(dev)
+            ss.wait_stream(torch.cuda.current_stream(dev))
+
+            def launch(k):
+                s = sets[k % len(sets)]
+                tw.tw_fused_reduce_residual_rmsnorm(s["plist"], s["R"], s["G"], 1e-5, s["out"],
+                                                    stream=ss, sm_budget=budget)
+
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(ss):
+                a.record(ss)
+                for k in range(reps):
+                    launch(k)
+                b.record(ss)
+                torch.cuda.synchronize()
+                b2b_us = a.elapsed_time(b) * 1e3 / reps
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=ss):
+                    for k in range(reps):
+                        launch(k)
+                g.replay()
+                torch.cuda.synchronize()
+                a.record(ss)
+                g.replay()
+                b.record(ss)
+                torch.cuda.synchronize()
+                graph_us = a.elapsed_time(b) * 1e3 / reps
+            del g
+            torch.cuda.current_stream(dev).wait_stream(ss)
+            extra = {"b2b_us": round(b2b_us, 2), "b2b_GB_s": round(bytes_call / b2b_us / 1e3, 1),
+                     "graph_us": round(graph_us, 2),
+                     "graph_GB_s": round(bytes_call / graph_us / 1e3, 1)}
             if budget == 0:
                 ucalls = [tw.UnfusedCall(s["plist"], s["R"], s["G"], 1e-5, s["out"]) for s in sets]
                 for k in range(3):
@@ -539,7 +638,8 @@ def sweep(args):
                     uevs[k][1].record()
                 torch.cuda.synchronize()
                 uus = sorted(a.elapsed_time(b) * 1e3 for a, b in uevs)[reps // 2]
-                extra = {"unfused_us_median": round(uus, 2), "fused_speedup": round(uus / med, 3)}
+                extra.update({"unfused_us_median": round(uus, 2),
+                              "fused_speedup": round(uus / med, 3)})
             print(json.dumps({"T": T, "H": H, "N": N, "sm_budget": budget or "full",
                               "sms_used": used, "us_median": round(med, 2),
                               "us_p10": round(us[len(us) // 10], 2),

@@ -1,6 +1,7 @@
 """bench.py's host-side helpers on the CPU: roofline denominator and its
 fallback, the ncu traffic record tied to the kernel source revision, the
-clock-record summary, and the split workload's CTA model."""
+clock-record summary, the split workload's CTA model, and the oracle timed
+over spawned shards."""
 
 import json
 
@@ -49,3 +50,14 @@ def test_cta_model_of_the_split_workload():
     # ceil(T/128) * (H/128) / 8: the configs' 64 / 128 / 256 / 512 CTAs
     assert [bench.ctas_unsplit(T, 8192) for T in (1024, 2048, 4096, 8192)] == [64, 128, 256, 512]
     assert bench.ctas_unsplit(4864, 8192) == 304
+
+
+def test_oracle_over_spawned_shards_covers_the_rows():
+    # PR1 (T=128): the budget covers every row, split into one contiguous
+    # shard per host core (at most 128 non-empty shards)
+    import os
+    r = bench.cpu_baseline_procs("pr1_t128_h4096_n2", 0, t_row_s=1e-4, budget_s=5.0)
+    assert r is not None
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0
+    assert r["cores"] == min(len(os.sched_getaffinity(0)), 128)
+    assert r["sample"].startswith("128 of 128 token rows")
