@@ -16,12 +16,12 @@
  *   - Launches are asynchronous on the stream(s) given; a device fault shows
  *     at the caller's next synchronisation, as usual in CUDA. Work runs on the
  *     device that is current on the calling thread.
- *   - Fused launches use programmatic dependent launch. Their thread blocks
- *     may become resident while the previous kernel on the stream is still
- *     running, and they ask L2 to prefetch the first bytes of their input
- *     rows, a hint that reads nothing into the step. Every load and store of
- *     the step happens after that kernel has completed, so stream order holds
- *     as for an ordinary launch.
+ *   - Every launch uses programmatic dependent launch: its thread blocks may
+ *     become resident while the previous kernel on the stream is still
+ *     running. The fused step's blocks then ask L2 to prefetch the first bytes
+ *     of their input rows, a hint that reads nothing into the step. Every
+ *     load and store of a launch happens after that kernel has completed, so
+ *     stream order holds as for an ordinary launch.
  *   - Arguments are validated before any CUDA call. Every call returns a
  *     tw_status; no C++ exception crosses this boundary.
  *   - A stream argument is a cudaStream_t; NULL is the legacy default stream.
