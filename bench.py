@@ -220,8 +220,10 @@ def gpu_arm(args, rank, world):
              for s in sets]
     graphs = {}
 
+    planner = tw.WaveSplitCall(C, PLANNER_SMS)
+
     def plan():
-        return tw.tw_wave_split(T, C, PLANNER_SMS)[0]
+        return planner(T)[0]
 
     def step_eager(k):
         calls[k % len(calls)](plan())
@@ -359,6 +361,7 @@ def e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb):
     run them: two device buffer sets, H2D on one stream, compute on another,
     D2H on a third, so step k's D2H overlaps step k+1's H2D (events order
     every reuse of a buffer set)."""
+    planner = tw.WaveSplitCall(C, PLANNER_SMS)
     import torch
     import synth
     w = dict(synth.WORKLOADS[args.workload])
@@ -391,7 +394,7 @@ def e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb):
             b["G"].copy_(hg, non_blocking=True)
             b["loaded"].record(s_h2d)
         sa.wait_event(b["loaded"])
-        b["call"](tw.tw_wave_split(T, C, PLANNER_SMS)[0])
+        b["call"](planner(T)[0])
         b["computed"].record(sa)
         s_d2h.wait_event(b["computed"])
         with torch.cuda.stream(s_d2h):

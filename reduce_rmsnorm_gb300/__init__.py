@@ -20,8 +20,9 @@ The functions carry the C names:
     tw_reduce_partials(partials, sum_out, stream=None)                 # unfused baseline
     tw_add_rmsnorm(sum_in, residual, gamma, eps, out, stream=None)     # unfused baseline
 
-For launch-bound loops, ``FusedCall`` and ``SplitCall`` marshal the arguments
-once and then launch with a single ctypes call each time they are called.
+For launch-bound loops, ``FusedCall``, ``SplitCall`` and ``WaveSplitCall``
+marshal the arguments once and then make a single ctypes call each time they
+are called.
 """
 
 import ctypes
@@ -281,13 +282,34 @@ class FusedCall:
         T, H = _shape(residual)
         self.tensors = (partials, residual, gamma, out)
         self._fn = lib().tw_fused_reduce_residual_rmsnorm
-        self._args = (arr, n, _ptr(residual), _ptr(gamma), ctypes.c_float(eps), T, H, _ptr(out),
-                      _stream(stream), int(sm_budget))
+        self._args = (arr, _int(n), _ptr(residual), _ptr(gamma), ctypes.c_float(eps), _i64(T),
+                      _i64(H), _ptr(out), _stream(stream), _int(int(sm_budget)))
 
     def __call__(self):
         st = self._fn(*self._args)
         if st != TW_OK:
             raise TwError(st, "tw_fused_reduce_residual_rmsnorm")
+
+
+class WaveSplitCall:
+    """tw_wave_split for fixed (ctas_unsplit, num_sms, options), marshalled
+    once: calling it with a token count returns (prefix_tokens,
+    suffix_tokens). The plan is still computed by the C planner on every
+    call."""
+
+    def __init__(self, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS,
+                 min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
+        self._opts, self._keep = _opts(offsets, min_split_tokens)
+        self._p, self._s = _i64(), _i64()
+        self._fn = lib().tw_wave_split
+        self._tail = (_i64(int(ctas_unsplit)), _int(int(num_sms)), ctypes.byref(self._opts),
+                      ctypes.byref(self._p), ctypes.byref(self._s))
+
+    def __call__(self, num_tokens):
+        st = self._fn(int(num_tokens), *self._tail)
+        if st != TW_OK:
+            raise TwError(st, "tw_wave_split")
+        return self._p.value, self._s.value
 
 
 class SplitCall:
@@ -301,8 +323,9 @@ class SplitCall:
         self.tokens = T
         self.tensors = (partials, residual, gamma, out)
         self._fn = lib().tw_run_split
-        self._args = (arr, n, _ptr(residual), _ptr(gamma), ctypes.c_float(eps), T, H, _ptr(out),
-                      _stream(stream_a), _stream(stream_b), int(sm_budget))
+        self._args = (arr, _int(n), _ptr(residual), _ptr(gamma), ctypes.c_float(eps), _i64(T),
+                      _i64(H), _ptr(out), _stream(stream_a), _stream(stream_b),
+                      _int(int(sm_budget)))
 
     def __call__(self, prefix_tokens):
         st = self._fn(int(prefix_tokens), *self._args)

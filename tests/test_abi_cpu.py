@@ -260,3 +260,20 @@ def test_split_lookup_rejects_bad_tables(L):
                              ctypes.byref(ctypes.c_int64())) == tw.TW_ERR_INVALID_ARG
     assert L.tw_split_lookup(None, None, -1, 10, 5, 4, None, ctypes.byref(p),
                              ctypes.byref(ctypes.c_int64())) == tw.TW_ERR_INVALID_ARG
+
+
+def test_prepared_planner_call_equals_the_planner(L):
+    """WaveSplitCall (arguments marshalled once) returns what tw_wave_split
+    returns, and what the brute-force oracle returns, for the default grid and
+    for every-integer offsets; bad arguments still raise."""
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        T = int(rng.integers(0, 6000))
+        C = int(rng.integers(0, 1200))
+        S = int(rng.integers(1, 300))
+        w = tw.WaveSplitCall(C, S)
+        assert w(T) == tw.tw_wave_split(T, C, S) == oplanner.wave_split(T, C, S)
+    w = tw.WaveSplitCall(300, 132, offsets=None, min_split_tokens=0)
+    assert w(300) == (132, 168)  # the guide's worked example, in CTA units
+    with pytest.raises(tw.TwError):
+        tw.WaveSplitCall(10, 0)(100)  # num_sms <= 0
