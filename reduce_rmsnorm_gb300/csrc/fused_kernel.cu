@@ -16,8 +16,9 @@
 //     (N <= 8) or 4 KiB of every source (N partials + residual), from HBM into
 //     a ring of shared-memory stages with 1-D TMA bulk copies (cp.async.bulk,
 //     mbarrier completion); lane r issues source r's copy, so the N + 1
-//     copies of a stage go out in parallel (one lane issuing them in turn, or
-//     4 KiB copies, caps an SM near 45 GB/s). Eight consumer warps
+//     copies of a stage go out in parallel (one lane issuing 4 KiB copies in
+//     turn capped an SM under an SM budget near 57 GB/s; now 8 KiB copies
+//     reach ~128 GB/s and 4 KiB copies 80-95 GB/s). Eight consumer warps
 //     read a chunk (one or two 16-byte vectors per thread per source), sum in
 //     fp32 in rank order (packed f32x2 adds), add the residual, store the
 //     updated residual, and keep z in registers.
