@@ -7,8 +7,11 @@
     python bench.py --offset-sweep [--sm-budget k]   # timed offset sweep -> lookup table
 
 A step is one pass of the hot path over one batch: the wave-aware split plan
-(tw_wave_split, host) and the fused step over the batch (tw_run_split: prefix
-on one stream, suffix on another; at T=1024 the plan keeps the batch whole).
+and the fused step over the batch, prefix on one stream, suffix on another
+(at T=1024 the plan keeps the batch whole). Eager steps make one C call,
+tw_run_wave_split, which computes the plan on the host every step and
+launches the halves; graph mode plans with tw_wave_split and replays the
+graph captured for that plan.
 The default workload is the Llama-3.3-70B layer shape, T=1024 tokens, H=8192,
 N=8 partial buffers. Inputs rotate among enough seeded sets to exceed 4x the
 L2 cache, so no step reads inputs the previous step left in L2.
@@ -25,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -53,9 +57,15 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sha():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_sha(path=None):
+    """Fingerprint of the kernel's code: its source with comments removed and
+    whitespace runs collapsed, so that editing prose keeps the ncu record
+    while any change to the code orphans it."""
+    with open(path or KERNEL_SRC) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.sha256(" ".join(src.split()).encode()).hexdigest()[:16]
 
 
 def ncu_traffic(workload):
@@ -218,6 +228,9 @@ def gpu_arm(args, rank, world):
     sb = torch.cuda.Stream(dev)
     calls = [tw.SplitCall(s["plist"], s["R"], s["G"], eps, s["out"], sa, sb, args.sm_budget)
              for s in sets]
+    # eager steps: one C call plans the split (every step) and runs it
+    planned = [tw.PlannedSplitCall(C, PLANNER_SMS, s["plist"], s["R"], s["G"], eps, s["out"], sa,
+                                   sb, args.sm_budget) for s in sets]
     graphs = {}
 
     planner = tw.WaveSplitCall(C, PLANNER_SMS)
@@ -226,7 +239,7 @@ def gpu_arm(args, rank, world):
         return planner(T)[0]
 
     def step_eager(k):
-        calls[k % len(calls)](plan())
+        planned[k % len(planned)]()
 
     def step_graph(k):
         # the plan is computed every step; the graph captured for this input
@@ -361,7 +374,6 @@ def e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb):
     run them: two device buffer sets, H2D on one stream, compute on another,
     D2H on a third, so step k's D2H overlaps step k+1's H2D (events order
     every reuse of a buffer set)."""
-    planner = tw.WaveSplitCall(C, PLANNER_SMS)
     import torch
     import synth
     w = dict(synth.WORKLOADS[args.workload])
@@ -379,8 +391,8 @@ def e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb):
         G = torch.empty_like(g, device=dev)
         out = torch.empty_like(R)
         bufs.append(dict(P=P, R=R, G=G, out=out,
-                         call=tw.SplitCall([P[i] for i in range(N)], R, G, eps, out, sa, sb,
-                                           args.sm_budget),
+                         call=tw.PlannedSplitCall(C, PLANNER_SMS, [P[i] for i in range(N)], R,
+                                                  G, eps, out, sa, sb, args.sm_budget),
                          loaded=torch.cuda.Event(), computed=torch.cuda.Event(),
                          drained=torch.cuda.Event()))
     steps = max(3, min(args.e2e_steps, args.steps))
@@ -394,7 +406,7 @@ def e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb):
             b["G"].copy_(hg, non_blocking=True)
             b["loaded"].record(s_h2d)
         sa.wait_event(b["loaded"])
-        b["call"](planner(T)[0])
+        b["call"]()
         b["computed"].record(sa)
         s_d2h.wait_event(b["computed"])
         with torch.cuda.stream(s_d2h):

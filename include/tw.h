@@ -203,6 +203,21 @@ TW_API int tw_run_split(int64_t prefix_tokens, const void* const* partials, int 
                  tw_stream_t stream_a, tw_stream_t stream_b, int sm_budget);
 
 /*
+ * tw_run_wave_split -- plan and run in one call: the wave-aware split
+ * tw_wave_split(T, ctas_unsplit, num_sms, opts), computed on every call
+ * ([W] "Fix one": the split is decided each iteration), then tw_run_split
+ * with that prefix. prefix_tokens and suffix_tokens (host pointers, each may
+ * be NULL) receive the plan. The fused arguments are validated first, then
+ * the planner's; both before any CUDA call. Arguments, ordering and errors
+ * otherwise as for tw_wave_split and tw_run_split.
+ */
+TW_API int tw_run_wave_split(int64_t ctas_unsplit, int num_sms, const tw_split_opts* opts,
+                      const void* const* partials, int N, void* residual, const void* gamma,
+                      float eps, int64_t T, int64_t H, void* out, tw_stream_t stream_a,
+                      tw_stream_t stream_b, int sm_budget, int64_t* prefix_tokens,
+                      int64_t* suffix_tokens);
+
+/*
  * tw_run_split_after -- the split step as the pages pipeline it against the
  * projection that produces the partials ([G] "Architectural Foundations of
  * TokenWeave" and "The Mathematics of Token-Splitting and Overlap": stream A

@@ -11,6 +11,8 @@ The functions carry the C names:
     tw_wave_split(num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS, min_split_tokens=1024)
     tw_split_lookup(table, num_tokens, ctas_unsplit, num_sms, offsets=..., min_split_tokens=...)
     tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a, stream_b, sm_budget=0)
+    tw_run_wave_split(ctas_unsplit, num_sms, partials, residual, gamma, eps, out, stream_a, stream_b,
+                      sm_budget=0, offsets=..., min_split_tokens=...)          # plan + run
     tw_run_split_after(prefix_tokens, partials, residual, gamma, eps, out, stream,
                        prefix_ready, suffix_ready, sm_budget=0)
     tw_strerror(status)
@@ -20,9 +22,9 @@ The functions carry the C names:
     tw_reduce_partials(partials, sum_out, stream=None)                 # unfused baseline
     tw_add_rmsnorm(sum_in, residual, gamma, eps, out, stream=None)     # unfused baseline
 
-For launch-bound loops, ``FusedCall``, ``SplitCall`` and ``WaveSplitCall``
-marshal the arguments once and then make a single ctypes call each time they
-are called.
+For launch-bound loops, ``FusedCall``, ``SplitCall``, ``WaveSplitCall`` and
+``PlannedSplitCall`` marshal the arguments once and then make a single ctypes
+call each time they are called.
 """
 
 import ctypes
@@ -45,7 +47,8 @@ DEFAULT_MIN_SPLIT_TOKENS = 1024
 
 EXPORTED = ("tw_fused_reduce_residual_rmsnorm", "tw_wave_split", "tw_run_split", "tw_strerror",
             "tw_launch_shape", "tw_device_status", "tw_fused_debug_smid", "tw_reduce_partials",
-            "tw_add_rmsnorm", "tw_run_split_after", "tw_split_lookup", "tw_debug_wait_timeout")
+            "tw_add_rmsnorm", "tw_run_split_after", "tw_split_lookup", "tw_debug_wait_timeout",
+            "tw_run_wave_split")
 
 
 class TwError(RuntimeError):
@@ -94,6 +97,10 @@ def lib():
     L.tw_run_split.argtypes = [_i64, ctypes.POINTER(_vp), _int, _vp, _vp, ctypes.c_float, _i64,
                                _i64, _vp, _vp, _vp, _int]
     L.tw_run_split.restype = _int
+    L.tw_run_wave_split.argtypes = [_i64, _int, ctypes.POINTER(_SplitOpts), ctypes.POINTER(_vp),
+                                    _int, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp, _vp,
+                                    _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
+    L.tw_run_wave_split.restype = _int
     L.tw_strerror.argtypes = [_int]
     L.tw_strerror.restype = ctypes.c_char_p
     L.tw_launch_shape.argtypes = [_i64, _i64, _int, _int] + [ctypes.POINTER(_int)] * 4
@@ -238,6 +245,24 @@ def tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a=No
     _check(st, "tw_run_split")
 
 
+def tw_run_wave_split(ctas_unsplit, num_sms, partials, residual, gamma, eps, out,
+                      stream_a=None, stream_b=None, sm_budget=0, offsets=DEFAULT_OFFSETS,
+                      min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
+    """The wave-aware plan and the split step in one C call; returns the plan
+    (prefix_tokens, suffix_tokens)."""
+    arr, n = _partials_array(partials)
+    T, H = _shape(residual)
+    opts, keep = _opts_cached(offsets, min_split_tokens)
+    p, s = _i64(), _i64()
+    st = lib().tw_run_wave_split(int(ctas_unsplit), int(num_sms), ctypes.byref(opts), arr, n,
+                                 _ptr(residual), _ptr(gamma), float(eps), T, H, _ptr(out),
+                                 _stream(stream_a), _stream(stream_b), int(sm_budget),
+                                 ctypes.byref(p), ctypes.byref(s))
+    del keep
+    _check(st, "tw_run_wave_split")
+    return p.value, s.value
+
+
 def _event(e):
     return None if e is None else ctypes.c_void_p(e.cuda_event if hasattr(e, "cuda_event") else int(e))
 
@@ -331,6 +356,33 @@ class SplitCall:
         st = self._fn(int(prefix_tokens), *self._args)
         if st != TW_OK:
             raise TwError(st, "tw_run_split")
+
+
+class PlannedSplitCall:
+    """tw_run_wave_split with its arguments marshalled once: each call plans
+    the split in C (the planner runs every time) and runs the step; it
+    returns the plan (prefix_tokens, suffix_tokens)."""
+
+    def __init__(self, ctas_unsplit, num_sms, partials, residual, gamma, eps, out,
+                 stream_a=None, stream_b=None, sm_budget=0, offsets=DEFAULT_OFFSETS,
+                 min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
+        arr, n = _partials_array(partials)
+        T, H = _shape(residual)
+        self.tokens = T
+        self.tensors = (partials, residual, gamma, out)
+        self._opts, self._keep = _opts(offsets, min_split_tokens)
+        self._p, self._s = _i64(), _i64()
+        self._fn = lib().tw_run_wave_split
+        self._args = (_i64(int(ctas_unsplit)), _int(int(num_sms)), ctypes.byref(self._opts), arr,
+                      _int(n), _ptr(residual), _ptr(gamma), ctypes.c_float(eps), _i64(T), _i64(H),
+                      _ptr(out), _stream(stream_a), _stream(stream_b), _int(int(sm_budget)),
+                      ctypes.byref(self._p), ctypes.byref(self._s))
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != TW_OK:
+            raise TwError(st, "tw_run_wave_split")
+        return self._p.value, self._s.value
 
 
 class UnfusedCall:

@@ -129,38 +129,69 @@ extern "C" int tw_fused_debug_smid(const void* const* partials, int N, void* res
   }
 }
 
+namespace {
+
+// The split runner on validated arguments (`a` is filled only when T > 0),
+// prefix_tokens in [0, T].
+int run_split(const tw::FusedArgs& a, int64_t T, int64_t prefix_tokens, tw_stream_t stream_a,
+              tw_stream_t stream_b, int sm_budget) {
+  if (T == 0) return TW_OK;
+  cudaStream_t sa = reinterpret_cast<cudaStream_t>(stream_a);
+  cudaStream_t sb = reinterpret_cast<cudaStream_t>(stream_b);
+  const int64_t suffix = T - prefix_tokens;
+  int st = TW_OK;
+  if (suffix == 0 || sa == sb) {
+    if (prefix_tokens > 0 &&
+        (st = tw::launch_fused(slice(a, 0, prefix_tokens), sa, sm_budget, nullptr)) != TW_OK)
+      return st;
+    if (suffix > 0)
+      return tw::launch_fused(slice(a, prefix_tokens, suffix), sa, sm_budget, nullptr);
+    return TW_OK;
+  }
+  cudaEvent_t fork = nullptr, join = nullptr;
+  if ((st = split_events(&fork, &join)) != TW_OK) return st;
+  if (cudaEventRecord(fork, sa) != cudaSuccess || cudaStreamWaitEvent(sb, fork, 0) != cudaSuccess)
+    return TW_ERR_CUDA;
+  if (prefix_tokens > 0 &&
+      (st = tw::launch_fused(slice(a, 0, prefix_tokens), sa, sm_budget, nullptr)) != TW_OK)
+    return st;
+  if ((st = tw::launch_fused(slice(a, prefix_tokens, suffix), sb, sm_budget, nullptr)) != TW_OK)
+    return st;
+  if (cudaEventRecord(join, sb) != cudaSuccess || cudaStreamWaitEvent(sa, join, 0) != cudaSuccess)
+    return TW_ERR_CUDA;
+  return TW_OK;
+}
+
+}  // namespace
+
 extern "C" int tw_run_split(int64_t prefix_tokens, const void* const* partials, int N,
                             void* residual, const void* gamma, float eps, int64_t T, int64_t H,
                             void* out, tw_stream_t stream_a, tw_stream_t stream_b, int sm_budget) {
   try {
     tw::FusedArgs a;
-    int st = validate(partials, N, residual, gamma, eps, T, H, out, sm_budget, &a);
+    const int st = validate(partials, N, residual, gamma, eps, T, H, out, sm_budget, &a);
     if (st != TW_OK) return st;
     if (prefix_tokens < 0 || prefix_tokens > T) return TW_ERR_INVALID_ARG;
-    if (T == 0) return TW_OK;
-    cudaStream_t sa = reinterpret_cast<cudaStream_t>(stream_a);
-    cudaStream_t sb = reinterpret_cast<cudaStream_t>(stream_b);
-    const int64_t suffix = T - prefix_tokens;
-    if (suffix == 0 || sa == sb) {
-      if (prefix_tokens > 0 &&
-          (st = tw::launch_fused(slice(a, 0, prefix_tokens), sa, sm_budget, nullptr)) != TW_OK)
-        return st;
-      if (suffix > 0)
-        return tw::launch_fused(slice(a, prefix_tokens, suffix), sa, sm_budget, nullptr);
-      return TW_OK;
-    }
-    cudaEvent_t fork = nullptr, join = nullptr;
-    if ((st = split_events(&fork, &join)) != TW_OK) return st;
-    if (cudaEventRecord(fork, sa) != cudaSuccess || cudaStreamWaitEvent(sb, fork, 0) != cudaSuccess)
-      return TW_ERR_CUDA;
-    if (prefix_tokens > 0 &&
-        (st = tw::launch_fused(slice(a, 0, prefix_tokens), sa, sm_budget, nullptr)) != TW_OK)
-      return st;
-    if ((st = tw::launch_fused(slice(a, prefix_tokens, suffix), sb, sm_budget, nullptr)) != TW_OK)
-      return st;
-    if (cudaEventRecord(join, sb) != cudaSuccess || cudaStreamWaitEvent(sa, join, 0) != cudaSuccess)
-      return TW_ERR_CUDA;
-    return TW_OK;
+    return run_split(a, T, prefix_tokens, stream_a, stream_b, sm_budget);
+  } catch (...) {
+    return TW_ERR_CUDA;
+  }
+}
+
+extern "C" int tw_run_wave_split(int64_t ctas_unsplit, int num_sms, const tw_split_opts* opts,
+                                 const void* const* partials, int N, void* residual,
+                                 const void* gamma, float eps, int64_t T, int64_t H, void* out,
+                                 tw_stream_t stream_a, tw_stream_t stream_b, int sm_budget,
+                                 int64_t* prefix_tokens, int64_t* suffix_tokens) {
+  try {
+    tw::FusedArgs a;
+    int st = validate(partials, N, residual, gamma, eps, T, H, out, sm_budget, &a);
+    if (st != TW_OK) return st;
+    int64_t prefix = 0, suffix = 0;
+    if ((st = tw_wave_split(T, ctas_unsplit, num_sms, opts, &prefix, &suffix)) != TW_OK) return st;
+    if (prefix_tokens) *prefix_tokens = prefix;
+    if (suffix_tokens) *suffix_tokens = suffix;
+    return run_split(a, T, prefix, stream_a, stream_b, sm_budget);
   } catch (...) {
     return TW_ERR_CUDA;
   }

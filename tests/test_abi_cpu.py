@@ -277,3 +277,29 @@ def test_prepared_planner_call_equals_the_planner(L):
     assert w(300) == (132, 168)  # the guide's worked example, in CTA units
     with pytest.raises(tw.TwError):
         tw.WaveSplitCall(10, 0)(100)  # num_sms <= 0
+
+
+def test_run_wave_split_validates_before_any_cuda_call(L):
+    """Plan + run in one call: the fused arguments are checked first, then the
+    planner's; an empty batch plans (0, 0) and launches nothing; the plan
+    outputs may be NULL. None of these needs a GPU."""
+    arr = (ctypes.c_void_p * 2)(0, 0)
+    eps = ctypes.c_float(1e-5)
+    p, s = ctypes.c_int64(-1), ctypes.c_int64(-1)
+    opts = ctypes.byref(tw._opts(tw.DEFAULT_OFFSETS, tw.DEFAULT_MIN_SPLIT_TOKENS)[0])
+    f = L.tw_run_wave_split
+    assert f(0, 148, opts, arr, 2, None, None, eps, 0, 16, None, None, None, 0,
+             ctypes.byref(p), ctypes.byref(s)) == tw.TW_OK
+    assert (p.value, s.value) == (0, 0)
+    assert f(0, 148, None, arr, 2, None, None, eps, 0, 16, None, None, None, 0, None, None) == tw.TW_OK
+    # fused arguments: N out of range, H not a multiple of 8, null pointers (T > 0)
+    assert f(8, 148, None, arr, 0, None, None, eps, 4, 16, None, None, None, 0, None, None) == \
+        tw.TW_ERR_INVALID_ARG
+    assert f(8, 148, None, arr, 2, None, None, eps, 4, 12, None, None, None, 0, None, None) == \
+        tw.TW_ERR_ALIGN
+    assert f(8, 148, None, arr, 2, None, None, eps, 4, 16, None, None, None, 0, None, None) == \
+        tw.TW_ERR_INVALID_ARG
+    # planner arguments, checked with valid fused arguments
+    for C, S in ((8, 0), (-1, 148)):
+        assert f(C, S, None, arr, 2, None, None, eps, 0, 16, None, None, None, 0, None, None) == \
+            tw.TW_ERR_INVALID_ARG

@@ -61,3 +61,14 @@ def test_oracle_over_spawned_shards_covers_the_rows():
     assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0
     assert r["cores"] == min(len(os.sched_getaffinity(0)), 128)
     assert r["sample"].startswith("128 of 128 token rows")
+
+
+def test_kernel_fingerprint_ignores_prose_only(tmp_path):
+    src = tmp_path / "k.cu"
+    src.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1;  // store\n}\n")
+    base = bench.kernel_sha(str(src))
+    src.write_text("// header, reworded\n/* a block\n comment */\n__global__ void k(int* p) {\n"
+                   "    p[0] = 1;\n}\n")
+    assert bench.kernel_sha(str(src)) == base       # comments and layout only
+    src.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 2;  // store\n}\n")
+    assert bench.kernel_sha(str(src)) != base       # the code changed

@@ -30,6 +30,10 @@ int main(void) {
   const void* parts[1] = {NULL};
   if (tw_fused_reduce_residual_rmsnorm(parts, 0, NULL, NULL, 1e-5f, 4, 16, NULL, NULL, 0) !=
       TW_ERR_INVALID_ARG) return 6;
+  /* plan + run in one call: an empty batch plans (0, 0) and launches nothing */
+  p = s = -1;
+  if (tw_run_wave_split(0, 148, NULL, parts, 1, NULL, NULL, 1e-5f, 0, 16, NULL, NULL, NULL, 0,
+                        &p, &s) != TW_OK || p != 0 || s != 0) return 7;
   puts("c abi ok");
   return 0;
 }

@@ -274,6 +274,31 @@ def test_uneven_split_bitwise(prefix, budget):
     assert_same(ref[1], out)
 
 
+@pytest.mark.parametrize("T", [128, 4096, 4864])
+def test_plan_and_run_in_one_call(T):
+    """tw_run_wave_split and the prepared PlannedSplitCall: the plan equals
+    the planner's (and the oracle's), and the rows equal the unsplit call's
+    bit for bit."""
+    C = math.ceil(T / 128) * (8192 // 128) // 8
+    plan = oplanner.wave_split(T, C, 148)
+    p, r, g = synth.make_inputs(T, 8192, 8, 0.02, seed=T + 3)
+    ref = run(p, r, g)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    assert tw.tw_run_wave_split(C, 148, P, R, G, EPS, out, sa, sb) == plan
+    sa.synchronize()
+    assert_same(ref[0], R)
+    assert_same(ref[1], out)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    call = tw.PlannedSplitCall(C, 148, P, R, G, EPS, out, sa, sb)
+    assert call() == plan
+    sa.synchronize()
+    assert_same(ref[0], R)
+    assert_same(ref[1], out)
+
+
 def test_split_same_stream():
     T = 300
     p, r, g = synth.make_inputs(T, 4096, 4, 0.02, seed=30)
