@@ -263,7 +263,7 @@ __device__ __forceinline__ uint4 pack8(const float a[8]) {
 // staged chunk, in rank order, residual last. `src` addresses the column in
 // source 0's chunk; source r's chunk is `cbytes` further per r. NT > 0: N is a
 // compile-time constant and all N + 1 shared loads issue before the first
-// add; NT == 0: runtime N.
+// add; NT == 0: runtime N, loads issued in groups of up to four.
 template <int NT>
 __device__ __forceinline__ void reduce_vector(uint32_t src, uint32_t cbytes, int n, float a[8]) {
   if constexpr (NT > 0) {
@@ -274,15 +274,27 @@ __device__ __forceinline__ void reduce_vector(uint32_t src, uint32_t cbytes, int
 #pragma unroll
     for (int r = 1; r <= NT; ++r) add8(q[r], a);
   } else {
+    // Sources 1..n (source n is the residual) in groups of four whose loads
+    // issue together, then the last one to three together, so no load waits
+    // alone. The adds keep rank order, so the sum is bitwise the same.
     load8(lds128(src), a);
     int r = 1;
-    for (; r + 3 < n; r += 4) {
+    for (; r + 3 <= n; r += 4) {
       const uint4 q0 = lds128(src + r * cbytes), q1 = lds128(src + (r + 1) * cbytes);
       const uint4 q2 = lds128(src + (r + 2) * cbytes), q3 = lds128(src + (r + 3) * cbytes);
       add8(q0, a); add8(q1, a); add8(q2, a); add8(q3, a);
     }
-    for (; r < n; ++r) add8(lds128(src + r * cbytes), a);
-    add8(lds128(src + n * cbytes), a);  // residual last
+    const int left = n + 1 - r;  // 0..3 sources after the full groups
+    if (left == 3) {
+      const uint4 q0 = lds128(src + r * cbytes), q1 = lds128(src + (r + 1) * cbytes);
+      const uint4 q2 = lds128(src + (r + 2) * cbytes);
+      add8(q0, a); add8(q1, a); add8(q2, a);
+    } else if (left == 2) {
+      const uint4 q0 = lds128(src + r * cbytes), q1 = lds128(src + (r + 1) * cbytes);
+      add8(q0, a); add8(q1, a);
+    } else if (left == 1) {
+      add8(lds128(src + r * cbytes), a);
+    }
   }
 }
 
