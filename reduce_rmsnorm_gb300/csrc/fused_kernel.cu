@@ -26,9 +26,9 @@
 //     combine of the 8 warp sums, rsqrtf, and Y = (z * r) * gamma stored with
 //     16-byte stores. The per-row arithmetic depends only on H, so every grid
 //     size (SM budget), split and shard gives bitwise the same rows.
-//   * L2 policy per call: when the output fits in a quarter of the L2, the
-//     loads are evict-first and the output is stored streaming; larger calls
-//     use the normal policy for both.
+//   * L2 policy per call: for N <= 2 or N >= 9 with an output of at most an
+//     eighth of the L2, evict-first loads and a streaming output; otherwise
+//     the normal policy for both.
 //   * Programmatic dependent launch: the CTAs set up their barriers while the
 //     previous kernel in the stream drains, ask L2 for the first ~144 KiB of
 //     their rows (a prefetch hint, when a CTA owns more than one row), then
@@ -77,7 +77,7 @@ struct Params {
   uint4* residual;
   uint4* out;
   int* smid_out;
-  int l2_stream;    // 1: evict-first loads and streaming output stores (output <= L2 / 4)
+  int l2_stream;    // 1: evict-first loads and streaming output stores (see launch_fused)
   uint32_t prefetch_bytes;  // per source, from the CTA's first row: L2 warm-up before the
                             // dependency wait (multiple of 16; 0 = none)
   long long rows;
@@ -368,10 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     // ring; lane r < N copies partial r, lane N the residual.
     if (lane > n) return;
     const unsigned lanes = n + 1 == 32 ? 0xffffffffu : ((1u << (n + 1)) - 1u);
-    // Small calls (output <= L2 / 4) load evict-first, larger ones with the
-    // normal policy. Measured on H = 4096-16384, N = 2-16: evict-first gains
-    // 0.7-4% while the output fits in a quarter of the L2 and loses 1.5-5%
-    // above it, where the inputs of a launch far exceed the L2.
+    // Evict-first or normal L2 policy for the loads, chosen per call on the
+    // host (launch_fused).
     const uint64_t policy = p.l2_stream ? l2_evict_first_policy() : l2_evict_normal_policy();
     const uint4* src_base = lane < n ? p.partials[lane] : p.residual;
     const long long items = (row1 - row0) * chunks;
@@ -472,12 +470,11 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
         else load8(__ldg(p.gamma + v), g);
 #pragma unroll
         for (int i = 0; i < 8; ++i) y[i] = (z[j][i] * rs) * g[i];
-        // Small calls store the output evict-first, with the loads: its lines
-        // drain during this launch rather than competing with the next
-        // launch's reads (+1-4% at output <= L2 / 4). With normal loads the
-        // store policy measured within 0.2%. A kernel that reads Y right after
-        // still finds it unless L2 needs the room. The residual keeps the
-        // default policy (evict-first there measured -1%).
+        // With evict-first loads the output is stored streaming too, so its
+        // lines drain during this launch; with normal loads the store policy
+        // measured within 0.2%. A kernel that reads Y right after still finds
+        // it unless L2 needs the room. The residual keeps the default policy
+        // (evict-first there measured -1%).
         if (p.l2_stream) __stcs(out_row + v, pack8(y));
         else out_row[v] = pack8(y);
       }
@@ -634,7 +631,15 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
   p.residual = static_cast<uint4*>(a.residual);
   p.out = static_cast<uint4*>(a.out);
   p.smid_out = smid_out;
-  p.l2_stream = a.rows * a.hidden * 2 <= static_cast<int64_t>(d->l2_bytes) / 4 ? 1 : 0;
+  // L2 policy per call, measured with the prefetch below in place (back to
+  // back, interleaved, on two GB300s): normal loads win for N = 3..8 at every
+  // size (+1-6% at T = 512-2048, H = 4096-16384); evict-first loads with a
+  // streaming output win for N <= 2 and N >= 9 while the output is at most an
+  // eighth of the L2 (+1-6% at T <= 1024, H = 8192), and lose above it.
+  p.l2_stream = (a.n <= 2 || a.n >= 9) &&
+                        a.rows * a.hidden * 2 <= static_cast<int64_t>(d->l2_bytes) / 8
+                    ? 1
+                    : 0;
   // About 144 KiB per CTA, shared among the N + 1 sources. Only when some CTA
   // owns more than one row: with one row per CTA no CTA starts early.
   p.prefetch_bytes = a.rows > shape.grid ? (kPrefetchPerCta / static_cast<uint32_t>(a.n + 1)) & ~15u
