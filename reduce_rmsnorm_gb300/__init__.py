@@ -158,6 +158,61 @@ def _shape(residual):
     return int(residual.shape[0]), int(residual.shape[1])
 
 
+_BF16 = None
+
+
+def _bad_tensor(t, name, shape):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        return TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        return ValueError("%s must be a contiguous bf16 CUDA tensor (got %s, %s, contiguous=%s)"
+                          % (name, t.dtype, t.device, t.is_contiguous()))
+    return ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _check_tensor(t, name, shape):
+    """A bf16, contiguous CUDA tensor of the given shape: the layout the C ABI
+    takes as a raw pointer (it cannot see dtypes or strides)."""
+    global _BF16
+    if _BF16 is None:
+        import torch
+        _BF16 = torch.bfloat16
+    try:
+        ok = t.dtype is _BF16 and t.is_cuda and t.is_contiguous() and t.shape == shape
+    except AttributeError:
+        ok = False
+    if not ok:
+        raise _bad_tensor(t, name, shape)
+
+
+def _step_args(partials, residual, gamma, out):
+    """Validated (pointer array, N, T, H) for a fused step's tensors. An
+    [N, T, H] stack is checked once and its N pointers are computed from its
+    base address and stride."""
+    import torch
+    T, H = _shape(residual)
+    _check_tensor(residual, "residual", (T, H))
+    _check_tensor(gamma, "gamma", (H,))
+    _check_tensor(out, "out", (T, H))
+    if isinstance(partials, torch.Tensor) and partials.dim() == 3:
+        n = int(partials.shape[0])
+        if not (partials.dtype is torch.bfloat16 and partials.is_cuda and
+                tuple(partials.shape[1:]) == (T, H) and
+                (T * H == 0 or (partials.stride(2) == 1 and (T <= 1 or partials.stride(1) == H)))):
+            raise ValueError("partials must be [N, %d, %d] bf16 CUDA with contiguous [T, H] "
+                             "slices (got %s, %s, shape %s, strides %s)"
+                             % (T, H, partials.dtype, partials.device, tuple(partials.shape),
+                                partials.stride()))
+        base, step = partials.data_ptr(), partials.stride(0) * 2
+        return (_vp * max(n, 1))(*[base + i * step for i in range(n)]), n, T, H
+    seq = [partials] if isinstance(partials, torch.Tensor) else list(partials)
+    for r, t in enumerate(seq):
+        _check_tensor(t, "partials[%d]" % r, (T, H))
+    arr, n = _partials_array(seq)
+    return arr, n, T, H
+
+
 # ------------------------------------------------------------------ entry points
 
 
@@ -168,8 +223,7 @@ def tw_fused_reduce_residual_rmsnorm(partials, residual, gamma, eps, out, stream
     residual (in/out), out: bf16 [T, H]; gamma: bf16 [H]. Shapes are read from
     ``residual``; layout and error rules are those of the C call.
     """
-    arr, n = _partials_array(partials)
-    T, H = _shape(residual)
+    arr, n, T, H = _step_args(partials, residual, gamma, out)
     st = lib().tw_fused_reduce_residual_rmsnorm(arr, n, _ptr(residual), _ptr(gamma), float(eps), T,
                                                 H, _ptr(out), _stream(stream), int(sm_budget))
     _check(st, "tw_fused_reduce_residual_rmsnorm")
@@ -177,8 +231,7 @@ def tw_fused_reduce_residual_rmsnorm(partials, residual, gamma, eps, out, stream
 
 def tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=None, sm_budget=0):
     """The fused call that also records each CTA's SM id into ``smid_out`` (int32)."""
-    arr, n = _partials_array(partials)
-    T, H = _shape(residual)
+    arr, n, T, H = _step_args(partials, residual, gamma, out)
     st = lib().tw_fused_debug_smid(arr, n, _ptr(residual), _ptr(gamma), float(eps), T, H, _ptr(out),
                                    _stream(stream), int(sm_budget), _ptr(smid_out))
     _check(st, "tw_fused_debug_smid")
@@ -238,8 +291,7 @@ def tw_split_lookup(table, num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OF
 def tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a=None, stream_b=None,
                  sm_budget=0):
     """Rows [0, prefix) on stream_a, [prefix, T) on stream_b; stream_a joins both."""
-    arr, n = _partials_array(partials)
-    T, H = _shape(residual)
+    arr, n, T, H = _step_args(partials, residual, gamma, out)
     st = lib().tw_run_split(int(prefix_tokens), arr, n, _ptr(residual), _ptr(gamma), float(eps), T,
                             H, _ptr(out), _stream(stream_a), _stream(stream_b), int(sm_budget))
     _check(st, "tw_run_split")
@@ -250,8 +302,7 @@ def tw_run_wave_split(ctas_unsplit, num_sms, partials, residual, gamma, eps, out
                       min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
     """The wave-aware plan and the split step in one C call; returns the plan
     (prefix_tokens, suffix_tokens)."""
-    arr, n = _partials_array(partials)
-    T, H = _shape(residual)
+    arr, n, T, H = _step_args(partials, residual, gamma, out)
     opts, keep = _opts_cached(offsets, min_split_tokens)
     p, s = _i64(), _i64()
     st = lib().tw_run_wave_split(int(ctas_unsplit), int(num_sms), ctypes.byref(opts), arr, n,
@@ -272,8 +323,7 @@ def tw_run_split_after(prefix_tokens, partials, residual, gamma, eps, out, strea
     """On `stream`: wait prefix_ready, fused step on rows [0, prefix); wait
     suffix_ready, fused step on rows [prefix, T). Events: torch.cuda.Event or
     raw cudaEvent_t handles."""
-    arr, n = _partials_array(partials)
-    T, H = _shape(residual)
+    arr, n, T, H = _step_args(partials, residual, gamma, out)
     st = lib().tw_run_split_after(int(prefix_tokens), arr, n, _ptr(residual), _ptr(gamma),
                                   float(eps), T, H, _ptr(out), _stream(stream),
                                   _event(prefix_ready), _event(suffix_ready), int(sm_budget))
@@ -282,8 +332,13 @@ def tw_run_split_after(prefix_tokens, partials, residual, gamma, eps, out, strea
 
 def tw_reduce_partials(partials, sum_out, stream=None):
     """Unfused baseline, kernel 1: sum_out <- bf16(sum of the partials)."""
-    arr, n = _partials_array(partials)
     T, H = _shape(sum_out)
+    _check_tensor(sum_out, "sum_out", (T, H))
+    seq = [partials[i] for i in range(partials.shape[0])] if hasattr(partials, "dim") and \
+        partials.dim() == 3 else list(partials)
+    for r, t in enumerate(seq):
+        _check_tensor(t, "partials[%d]" % r, (T, H))
+    arr, n = _partials_array(seq)
     st = lib().tw_reduce_partials(arr, n, T, H, _ptr(sum_out), _stream(stream))
     _check(st, "tw_reduce_partials")
 
@@ -291,6 +346,9 @@ def tw_reduce_partials(partials, sum_out, stream=None):
 def tw_add_rmsnorm(sum_in, residual, gamma, eps, out, stream=None):
     """Unfused baseline, kernel 2: residual <- bf16(sum + residual); out <- RMSNorm(residual)."""
     T, H = _shape(residual)
+    for name, t, shape in (("sum_in", sum_in, (T, H)), ("residual", residual, (T, H)),
+                           ("gamma", gamma, (H,)), ("out", out, (T, H))):
+        _check_tensor(t, name, shape)
     st = lib().tw_add_rmsnorm(_ptr(sum_in), _ptr(residual), _ptr(gamma), float(eps), T, H,
                               _ptr(out), _stream(stream))
     _check(st, "tw_add_rmsnorm")
@@ -303,8 +361,7 @@ class FusedCall:
     the stream resolved at construction."""
 
     def __init__(self, partials, residual, gamma, eps, out, stream=None, sm_budget=0):
-        arr, n = _partials_array(partials)
-        T, H = _shape(residual)
+        arr, n, T, H = _step_args(partials, residual, gamma, out)
         self.tensors = (partials, residual, gamma, out)
         self._fn = lib().tw_fused_reduce_residual_rmsnorm
         self._args = (arr, _int(n), _ptr(residual), _ptr(gamma), ctypes.c_float(eps), _i64(T),
@@ -343,8 +400,7 @@ class SplitCall:
 
     def __init__(self, partials, residual, gamma, eps, out, stream_a=None, stream_b=None,
                  sm_budget=0):
-        arr, n = _partials_array(partials)
-        T, H = _shape(residual)
+        arr, n, T, H = _step_args(partials, residual, gamma, out)
         self.tokens = T
         self.tensors = (partials, residual, gamma, out)
         self._fn = lib().tw_run_split
@@ -366,8 +422,7 @@ class PlannedSplitCall:
     def __init__(self, ctas_unsplit, num_sms, partials, residual, gamma, eps, out,
                  stream_a=None, stream_b=None, sm_budget=0, offsets=DEFAULT_OFFSETS,
                  min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
-        arr, n = _partials_array(partials)
-        T, H = _shape(residual)
+        arr, n, T, H = _step_args(partials, residual, gamma, out)
         self.tokens = T
         self.tensors = (partials, residual, gamma, out)
         self._opts, self._keep = _opts(offsets, min_split_tokens)
@@ -391,8 +446,7 @@ class UnfusedCall:
     ``out`` in place (two launches)."""
 
     def __init__(self, partials, residual, gamma, eps, out, stream=None):
-        arr, n = _partials_array(partials)
-        T, H = _shape(residual)
+        arr, n, T, H = _step_args(partials, residual, gamma, out)
         self.tensors = (partials, residual, gamma, out)
         L = lib()
         s = _stream(stream)

@@ -303,3 +303,22 @@ def test_run_wave_split_validates_before_any_cuda_call(L):
     for C, S in ((8, 0), (-1, 148)):
         assert f(C, S, None, arr, 2, None, None, eps, 0, 16, None, None, None, 0, None, None) == \
             tw.TW_ERR_INVALID_ARG
+
+
+def test_binding_rejects_tensors_the_abi_cannot_describe():
+    """The C ABI takes raw pointers, so the binding checks what a pointer
+    cannot carry: host tensors are refused before any library call."""
+    import torch
+    P = torch.zeros(2, 4, 16, dtype=torch.bfloat16)
+    R = torch.zeros(4, 16, dtype=torch.bfloat16)
+    G = torch.ones(16, dtype=torch.bfloat16)
+    out = torch.empty_like(R)
+    for call in (lambda: tw.tw_fused_reduce_residual_rmsnorm(P, R, G, 1e-5, out),
+                 lambda: tw.tw_run_split(2, P, R, G, 1e-5, out),
+                 lambda: tw.tw_run_wave_split(8, 148, P, R, G, 1e-5, out),
+                 lambda: tw.FusedCall(P, R, G, 1e-5, out),
+                 lambda: tw.PlannedSplitCall(8, 148, P, R, G, 1e-5, out),
+                 lambda: tw.tw_reduce_partials(P, out),
+                 lambda: tw.tw_add_rmsnorm(out, R, G, 1e-5, out)):
+        with pytest.raises(ValueError, match="contiguous bf16 CUDA tensor"):
+            call()

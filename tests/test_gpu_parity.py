@@ -189,6 +189,21 @@ def test_empty_batch():
     torch.cuda.synchronize()
 
 
+def test_binding_rejects_wrong_dtype_shape_or_strides():
+    p, r, g = synth.make_inputs(4, 4096, 2, 0.02)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    with pytest.raises(ValueError, match="partials"):
+        tw.tw_fused_reduce_residual_rmsnorm(P.float(), R, G, EPS, out)       # fp32 partials
+    with pytest.raises(ValueError, match="gamma"):
+        tw.tw_fused_reduce_residual_rmsnorm(P, R, G[:2048], EPS, out)        # gamma of H/2
+    with pytest.raises(ValueError, match="out"):
+        tw.tw_fused_reduce_residual_rmsnorm(P, R, G, EPS, out.t())           # transposed view
+    with pytest.raises(ValueError, match="partials"):
+        tw.tw_fused_reduce_residual_rmsnorm([P[0], P[1][:, :2048]], R, G, EPS, out)  # [T, H/2]
+    assert_same(R, to_gpu(p, r, g)[1])                                        # nothing ran
+
+
 def test_misaligned_pointer_rejected_on_device_tensors():
     p, r, g = synth.make_inputs(4, 4096, 2, 0.02)
     P, R, G = to_gpu(p, r, g)
