@@ -40,9 +40,11 @@ def _inputs(T, H, N, L, seed):
     return p, extra, r, g
 
 
-def _chain(p, extra, r, g, L, sm_budget, sync):
+def _chain(p, extra, r, g, L, sm_budget, sync, split=False):
     """Runs the chain on a created stream; returns (final R, [Y_l], snapshots).
-    With sync, every step's inputs and results are copied to the host."""
+    With sync, every step's inputs and results are copied to the host. With
+    split, each step is the planned split step (tw_run_wave_split: plan on the
+    host, halves on two streams, joined on the first)."""
     dev = torch.device("cuda", 0)
     P0 = p.to(dev)
     E = [e.to(dev) for e in extra]
@@ -51,14 +53,21 @@ def _chain(p, extra, r, g, L, sm_budget, sync):
     outs = [torch.empty_like(R) for _ in range(L)]
     torch.cuda.synchronize()
     s = torch.cuda.Stream(dev)
+    s2 = torch.cuda.Stream(dev)
+    T, H = R.shape
+    ctas = -(-T // 128) * (H // 128) // 8
     snaps = []
     with torch.cuda.stream(s):
         for l in range(L):
             plist = [P0[i] for i in range(P0.shape[0])] if l == 0 else [outs[l - 1]] + list(E[l - 1])
             if sync:
                 before = (torch.stack([x.cpu() for x in plist]), R.cpu())
-            tw.tw_fused_reduce_residual_rmsnorm(plist, R, G, EPS, outs[l], stream=s,
-                                                sm_budget=sm_budget)
+            if split:
+                tw.tw_run_wave_split(ctas, 148, plist, R, G, EPS, outs[l], s, s2,
+                                     sm_budget=sm_budget)
+            else:
+                tw.tw_fused_reduce_residual_rmsnorm(plist, R, G, EPS, outs[l], stream=s,
+                                                    sm_budget=sm_budget)
             if sync:
                 torch.cuda.synchronize()
                 snaps.append((before[0], before[1], R.cpu(), outs[l].cpu()))
@@ -67,20 +76,22 @@ def _chain(p, extra, r, g, L, sm_budget, sync):
 
 
 CASES = [
-    # T, H, N, layers, sm_budget
-    (512, 8192, 8, 6, 0),      # 3-4 rows per CTA: CTAs of the next step start early
-    (1024, 8192, 8, 6, 0),     # the Llama-3.3-70B layer shape
-    (333, 4104, 3, 5, 0),      # ragged rows and chunks, runtime N
-    (128, 4096, 2, 8, 0),      # the PR1 shape: one row per CTA
-    (256, 8192, 8, 4, 8),      # under an SM budget of 8
+    # T, H, N, layers, sm_budget, planned split step
+    (512, 8192, 8, 6, 0, False),     # 3-4 rows per CTA: CTAs of the next step start early
+    (1024, 8192, 8, 6, 0, False),    # the Llama-3.3-70B layer shape
+    (333, 4104, 3, 5, 0, False),     # ragged rows and chunks, runtime N
+    (128, 4096, 2, 8, 0, False),     # the PR1 shape: one row per CTA
+    (256, 8192, 8, 4, 8, False),     # under an SM budget of 8
+    (4096, 8192, 8, 3, 0, True),     # planned 2048/2048 split on two streams, per step
+    (4864, 8192, 2, 3, 16, True),    # uneven planned split under a budget
 ]
 
 
-@pytest.mark.parametrize("T,H,N,L,budget", CASES)
-def test_chain_back_to_back_equals_synchronised(T, H, N, L, budget):
+@pytest.mark.parametrize("T,H,N,L,budget,split", CASES)
+def test_chain_back_to_back_equals_synchronised(T, H, N, L, budget, split):
     p, extra, r, g = _inputs(T, H, N, L, seed=T + 31 * N)
-    R_a, outs_a, _, _ = _chain(p, extra, r, g, L, budget, sync=False)
-    R_b, outs_b, snaps, g_cpu = _chain(p, extra, r, g, L, budget, sync=True)
+    R_a, outs_a, _, _ = _chain(p, extra, r, g, L, budget, sync=False, split=split)
+    R_b, outs_b, snaps, g_cpu = _chain(p, extra, r, g, L, budget, sync=True, split=split)
     for l in range(L):
         assert torch.equal(outs_a[l].view(torch.int16), outs_b[l].view(torch.int16)), \
             "step %d differs back to back" % l
