@@ -5,11 +5,14 @@
 
 Translation units compile in parallel into ``_build/`` (git-ignored), then
 link into ``reduce_rmsnorm_gb300/libtw.so``. The CUDA runtime is linked
-statically, so the library needs only the driver at run time.
+statically, so the library needs only the driver at run time. Processes that
+build at once (the ranks of a torchrun job) take an exclusive file lock in
+turn; whoever gets it second finds the library up to date.
 """
 
 import argparse
 import concurrent.futures
+import fcntl
 import hashlib
 import os
 import subprocess
@@ -47,15 +50,28 @@ def _digest():
     return h.hexdigest()
 
 
+def _up_to_date(stamp, digest):
+    if not (os.path.exists(LIB) and os.path.exists(stamp)):
+        return False
+    with open(stamp) as f:
+        return f.read().strip() == digest
+
+
 def build(force=False, verbose=False, ptxas_verbose=False):
     """Compile and link libtw.so; returns its path."""
     os.makedirs(BUILD, exist_ok=True)
     stamp = os.path.join(BUILD, "stamp")
     digest = _digest()
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
-        with open(stamp) as f:
-            if f.read().strip() == digest:
-                return LIB
+    if not force and _up_to_date(stamp, digest):
+        return LIB
+    with open(os.path.join(BUILD, "lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)  # released when the file closes
+        if not force and _up_to_date(stamp, digest):
+            return LIB  # another process built it meanwhile
+        return _build_locked(stamp, digest, verbose, ptxas_verbose)
+
+
+def _build_locked(stamp, digest, verbose, ptxas_verbose):
     nvcc = _nvcc()
 
     def compile_one(src):
@@ -75,7 +91,7 @@ def build(force=False, verbose=False, ptxas_verbose=False):
             if err:
                 sys.stderr.write(err)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = "%s.tmp%d" % (LIB, os.getpid())
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
