@@ -555,7 +555,8 @@ def reference_arm(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "T": T, "H": H, "N": N, "rows_per_step": rows},
+            "config": {"workload": args.workload, "T": T, "H": H, "N": N, "eps": 1e-5,
+                       "rows_per_step": rows},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
