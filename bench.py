@@ -448,16 +448,24 @@ def _oracle_rows_timer(workload, T_override):
         w["T"] = T_override
     T, H, N = w["T"], w["H"], w["N"]
 
-    def time_rows(n_rows, seed=0):
+    def sample(n_rows, seed=0):
         ww = dict(w)
         ww["T"] = n_rows
         p, r, g = synth.make_inputs(seed=seed, **ww)
-        pb, rb, gb = synth.bits(p), synth.bits(r), synth.bits(g)
+        return synth.bits(p), synth.bits(r), synth.bits(g)
+
+    def time_bits(bits):
+        pb, rb, gb = bits
         t0 = time.perf_counter()
         fused.reduce_residual_rmsnorm(pb, rb, gb, 1e-5)
         fused.residual_fp32_rank_order(pb, rb)
         return time.perf_counter() - t0
 
+    def time_rows(n_rows, seed=0):
+        return time_bits(sample(n_rows, seed))
+
+    time_rows.sample = sample
+    time_rows.time_bits = time_bits
     return T, H, N, time_rows
 
 
@@ -541,16 +549,23 @@ def reference_arm(args, rank, world):
         return None
     import reduce_rmsnorm_gb300 as tw
     T, H, N, time_rows = _oracle_rows_timer(args.workload, args.tokens)
-    t1 = time_rows(8) / 8
+    # cost of one oracle call on n rows ~ fixed + n * per_row, both measured,
+    # so that many short steps also fit the budget
+    t8 = time_rows(8)
+    t1 = time_rows(1)
+    per_row = max((t8 - t1) / 7, 1e-7)
+    fixed = max(t1 - per_row, 0.0)
     total_budget_s = 90.0
-    rows = int(max(1, min(T, total_budget_s / (args.steps + args.warmup) / max(t1, 1e-6))))
-    for k in range(args.warmup):
-        time_rows(rows, seed=k)
-    secs = [time_rows(rows, seed=args.warmup + k) for k in range(args.steps)]
+    per_step = total_budget_s / (args.steps + args.warmup)
+    rows = int(max(1, min(T, (per_step - fixed) / per_row)))
+    bits = time_rows.sample(rows)   # one sample, timed every step
+    for _ in range(args.warmup):
+        time_rows.time_bits(bits)
+    secs = [time_rows.time_bits(bits) for _ in range(args.steps)]
     total = sum(secs)
     value = tw.bytes_per_call(rows, H, N) * args.steps / total / 1e9
-    sample = "first %d of %d token rows of %s per step (fp64 NumPy oracle, one process)" % (
-        rows, T, args.workload)
+    sample = ("the same %d of %d token rows of %s every step (fp64 NumPy oracle, one process)"
+              % (rows, T, args.workload))
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
