@@ -72,3 +72,21 @@ def test_kernel_fingerprint_ignores_prose_only(tmp_path):
     assert bench.kernel_sha(str(src)) == base       # comments and layout only
     src.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 2;  // store\n}\n")
     assert bench.kernel_sha(str(src)) != base       # the code changed
+
+
+def test_reference_arm_line_on_the_oracle():
+    """The reference arm times the oracle only: its line carries impl,
+    the GPU arm's metric and workload, a cpu_baseline with cores 1, a
+    zero-copy e2e and no GPU launches; other ranks return nothing."""
+    import argparse
+    args = argparse.Namespace(workload="pr1_t128_h4096_n2", tokens=0, steps=3, warmup=3)
+    line = bench.reference_arm(args, 0, 1)
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "GB/s" and line["higher_is_better"] is True and line["value"] > 0
+    assert line["config"]["workload"] == "pr1_t128_h4096_n2"
+    assert 1 <= line["config"]["rows_per_step"] <= 128
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["gpu_launches"] == 0 and line["steps"] == 3
+    assert bench.reference_arm(args, 1, 2) is None
