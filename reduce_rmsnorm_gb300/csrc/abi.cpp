@@ -12,10 +12,10 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool overlap(const void* a, const void* b, int64_t bytes) {
+// Whether [a, a + na) and [b, b + nb) share a byte.
+bool overlap(const void* a, int64_t na, const void* b, int64_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  const uintptr_t n = static_cast<uintptr_t>(bytes);
-  return x < y + n && y < x + n;
+  return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
 }
 
 // Checks that do not look at pointers (shared by the launch-shape query).
@@ -47,11 +47,11 @@ int validate(const void* const* partials, int N, void* residual, const void* gam
   // other), except that out may be exactly one partial's buffer: a row's
   // partial chunks are all staged before the row's output is written, and
   // staging runs ahead only into later rows.
-  if (overlap(residual, out, bytes)) return TW_ERR_INVALID_ARG;
+  if (overlap(residual, bytes, out, bytes)) return TW_ERR_INVALID_ARG;
   for (void* w : {residual, out}) {
-    if (overlap(w, gamma, H * 2)) return TW_ERR_INVALID_ARG;
+    if (overlap(w, bytes, gamma, H * 2)) return TW_ERR_INVALID_ARG;
     for (int r = 0; r < N; ++r)
-      if (overlap(w, partials[r], bytes) && !(w == out && out == partials[r]))
+      if (overlap(w, bytes, partials[r], bytes) && !(w == out && out == partials[r]))
         return TW_ERR_INVALID_ARG;
   }
   for (int r = 0; r < N; ++r) a->partials[r] = partials[r];
@@ -238,7 +238,7 @@ extern "C" int tw_reduce_partials(const void* const* partials, int N, int64_t T,
     if (!aligned16(sum_out)) return TW_ERR_ALIGN;
     const int64_t bytes = T * H * 2;
     for (int r = 0; r < N; ++r)
-      if (overlap(sum_out, partials[r], bytes)) return TW_ERR_INVALID_ARG;
+      if (overlap(sum_out, bytes, partials[r], bytes)) return TW_ERR_INVALID_ARG;
     return tw::launch_reduce(partials, N, T, H, sum_out, reinterpret_cast<cudaStream_t>(stream));
   } catch (...) {
     return TW_ERR_CUDA;
@@ -254,9 +254,11 @@ extern "C" int tw_add_rmsnorm(const void* sum, void* residual, const void* gamma
     if (!aligned16(sum) || !aligned16(residual) || !aligned16(gamma) || !aligned16(out))
       return TW_ERR_ALIGN;
     const int64_t bytes = T * H * 2;
-    if (overlap(residual, out, bytes) || overlap(residual, sum, bytes)) return TW_ERR_INVALID_ARG;
-    if (overlap(residual, gamma, H * 2) || overlap(out, gamma, H * 2)) return TW_ERR_INVALID_ARG;
-    if (sum != out && overlap(sum, out, bytes)) return TW_ERR_INVALID_ARG;  // same buffer is fine
+    if (overlap(residual, bytes, out, bytes) || overlap(residual, bytes, sum, bytes))
+      return TW_ERR_INVALID_ARG;
+    if (overlap(residual, bytes, gamma, H * 2) || overlap(out, bytes, gamma, H * 2))
+      return TW_ERR_INVALID_ARG;
+    if (sum != out && overlap(sum, bytes, out, bytes)) return TW_ERR_INVALID_ARG;  // same buffer is fine
     return tw::launch_add_rmsnorm(sum, residual, gamma, eps, T, H, out,
                                   reinterpret_cast<cudaStream_t>(stream));
   } catch (...) {

@@ -205,6 +205,10 @@ def test_validation_overlaps(L):
     # the residual may not alias a partial, even exactly
     assert _fused(L, T=T, H=H, residual=BASE + (1 << 24)) == tw.TW_ERR_INVALID_ARG
     assert _fused(L, T=T, H=H, residual=BASE + (41 << 24) - 16) == tw.TW_ERR_INVALID_ARG
+    # gamma inside a written tensor beyond its first row is rejected too
+    # (the residual spans T rows, gamma one row of H values)
+    assert _fused(L, T=T, H=H, gamma=r + 2 * H * 2) == tw.TW_ERR_INVALID_ARG
+    assert _fused(L, T=T, H=H, gamma=BASE + (42 << 24) + 3 * H * 2) == tw.TW_ERR_INVALID_ARG
     # partials aliasing one another is allowed by validation (reads only):
     # the call gets past validation and fails only at the first CUDA call
     # when there is no GPU, or launches when there is one -- not run here.
