@@ -237,17 +237,17 @@ def tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=No
     _check(st, "tw_fused_debug_smid")
 
 
-_default_opts = None
 
 
-def _opts_cached(offsets, min_split_tokens):
-    """Split options as a ctypes struct; the pages' defaults are built once."""
-    global _default_opts
-    if offsets is DEFAULT_OFFSETS and min_split_tokens == DEFAULT_MIN_SPLIT_TOKENS:
-        if _default_opts is None:
-            _default_opts = _opts(offsets, min_split_tokens)
-        return _default_opts
-    return _opts(offsets, min_split_tokens)
+def _opts_arg(offsets, min_split_tokens):
+    """(options pointer, objects to keep alive) for the C planner. The pages'
+    defaults go as NULL, which the planner serves from its own static list."""
+    if (offsets is DEFAULT_OFFSETS or (offsets is not None and
+                                       tuple(offsets) == tuple(DEFAULT_OFFSETS))) and \
+            min_split_tokens == DEFAULT_MIN_SPLIT_TOKENS:
+        return None, None
+    opts, keep = _opts(offsets, min_split_tokens)
+    return ctypes.byref(opts), (opts, keep)
 
 
 def tw_wave_split(num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS,
@@ -256,9 +256,9 @@ def tw_wave_split(num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS,
 
     offsets=None means every integer offset 0 .. half-1.
     """
-    opts, keep = _opts_cached(offsets, min_split_tokens)
+    optp, keep = _opts_arg(offsets, min_split_tokens)
     p, s = _i64(), _i64()
-    st = lib().tw_wave_split(int(num_tokens), int(ctas_unsplit), int(num_sms), ctypes.byref(opts),
+    st = lib().tw_wave_split(int(num_tokens), int(ctas_unsplit), int(num_sms), optp,
                              ctypes.byref(p), ctypes.byref(s))
     del keep
     _check(st, "tw_wave_split")
@@ -279,10 +279,10 @@ def tw_split_lookup(table, num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OF
     items = sorted(table.items())
     toks = (_i64 * max(len(items), 1))(*[int(k) for k, _ in items])
     pref = (_i64 * max(len(items), 1))(*[int(v) for _, v in items])
-    opts, keep = _opts(offsets, min_split_tokens)
+    optp, keep = _opts_arg(offsets, min_split_tokens)
     p, s = _i64(), _i64()
     st = lib().tw_split_lookup(toks, pref, len(items), int(num_tokens), int(ctas_unsplit),
-                               int(num_sms), ctypes.byref(opts), ctypes.byref(p), ctypes.byref(s))
+                               int(num_sms), optp, ctypes.byref(p), ctypes.byref(s))
     del keep
     _check(st, "tw_split_lookup")
     return p.value, s.value
@@ -303,9 +303,9 @@ def tw_run_wave_split(ctas_unsplit, num_sms, partials, residual, gamma, eps, out
     """The wave-aware plan and the split step in one C call; returns the plan
     (prefix_tokens, suffix_tokens)."""
     arr, n, T, H = _step_args(partials, residual, gamma, out)
-    opts, keep = _opts_cached(offsets, min_split_tokens)
+    optp, keep = _opts_arg(offsets, min_split_tokens)
     p, s = _i64(), _i64()
-    st = lib().tw_run_wave_split(int(ctas_unsplit), int(num_sms), ctypes.byref(opts), arr, n,
+    st = lib().tw_run_wave_split(int(ctas_unsplit), int(num_sms), optp, arr, n,
                                  _ptr(residual), _ptr(gamma), float(eps), T, H, _ptr(out),
                                  _stream(stream_a), _stream(stream_b), int(sm_budget),
                                  ctypes.byref(p), ctypes.byref(s))
@@ -381,10 +381,10 @@ class WaveSplitCall:
 
     def __init__(self, ctas_unsplit, num_sms, offsets=DEFAULT_OFFSETS,
                  min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
-        self._opts, self._keep = _opts(offsets, min_split_tokens)
+        optp, self._keep = _opts_arg(offsets, min_split_tokens)
         self._p, self._s = _i64(), _i64()
         self._fn = lib().tw_wave_split
-        self._tail = (_i64(int(ctas_unsplit)), _int(int(num_sms)), ctypes.byref(self._opts),
+        self._tail = (_i64(int(ctas_unsplit)), _int(int(num_sms)), optp,
                       ctypes.byref(self._p), ctypes.byref(self._s))
 
     def __call__(self, num_tokens):
@@ -425,10 +425,10 @@ class PlannedSplitCall:
         arr, n, T, H = _step_args(partials, residual, gamma, out)
         self.tokens = T
         self.tensors = (partials, residual, gamma, out)
-        self._opts, self._keep = _opts(offsets, min_split_tokens)
+        optp, self._keep = _opts_arg(offsets, min_split_tokens)
         self._p, self._s = _i64(), _i64()
         self._fn = lib().tw_run_wave_split
-        self._args = (_i64(int(ctas_unsplit)), _int(int(num_sms)), ctypes.byref(self._opts), arr,
+        self._args = (_i64(int(ctas_unsplit)), _int(int(num_sms)), optp, arr,
                       _int(n), _ptr(residual), _ptr(gamma), ctypes.c_float(eps), _i64(T), _i64(H),
                       _ptr(out), _stream(stream_a), _stream(stream_b), _int(int(sm_budget)),
                       ctypes.byref(self._p), ctypes.byref(self._s))

@@ -20,7 +20,7 @@
 
 namespace {
 
-const int kDefaultOffsets[] = {0, 64, 128, 192, 256, 512};
+const int64_t kDefaultOffsets[] = {0, 64, 128, 192, 256, 512};  // sorted, unique
 const int kDefaultMinSplitTokens = 1024;
 
 int64_t ceil_div(int64_t a, int64_t b) { return a / b + (a % b != 0); }  // a >= 0, b > 0
@@ -40,7 +40,11 @@ extern "C" int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_s
   if (num_tokens < 0 || ctas_unsplit < 0 || num_sms <= 0) return TW_ERR_INVALID_ARG;
 
   bool every_offset = false;
-  std::vector<int64_t> offsets(std::begin(kDefaultOffsets), std::end(kDefaultOffsets));
+  // The default offsets are used in place; a caller's list is copied, sorted
+  // and deduplicated (no exception leaves this function).
+  const int64_t* offsets = kDefaultOffsets;
+  size_t n_offsets = sizeof(kDefaultOffsets) / sizeof(kDefaultOffsets[0]);
+  std::vector<int64_t> custom;
   int64_t min_split = kDefaultMinSplitTokens;
   if (opts) {
     if (opts->n_offsets < 0) return TW_ERR_INVALID_ARG;
@@ -48,9 +52,17 @@ extern "C" int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_s
     if (!opts->offsets) {
       every_offset = true;
     } else {
-      offsets.assign(opts->offsets, opts->offsets + opts->n_offsets);
-      for (int64_t o : offsets)
-        if (o < 0) return TW_ERR_INVALID_ARG;
+      for (int i = 0; i < opts->n_offsets; ++i)
+        if (opts->offsets[i] < 0) return TW_ERR_INVALID_ARG;
+      try {
+        custom.assign(opts->offsets, opts->offsets + opts->n_offsets);
+      } catch (...) {
+        return TW_ERR_INVALID_ARG;  // a list too large to copy
+      }
+      std::sort(custom.begin(), custom.end());
+      custom.erase(std::unique(custom.begin(), custom.end()), custom.end());
+      offsets = custom.data();
+      n_offsets = custom.size();
     }
     min_split = opts->min_split_tokens;
   }
@@ -83,11 +95,9 @@ extern "C" int tw_wave_split(int64_t num_tokens, int64_t ctas_unsplit, int num_s
       if (try_offset(off)) return TW_OK;
     return TW_OK;
   }
-  std::sort(offsets.begin(), offsets.end());
-  offsets.erase(std::unique(offsets.begin(), offsets.end()), offsets.end());
-  for (int64_t off : offsets) {
-    if (off >= half) break;
-    if (try_offset(off)) return TW_OK;
+  for (size_t i = 0; i < n_offsets; ++i) {
+    if (offsets[i] >= half) break;
+    if (try_offset(offsets[i])) return TW_OK;
   }
   return TW_OK;
 }
