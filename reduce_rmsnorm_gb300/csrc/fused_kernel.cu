@@ -504,22 +504,29 @@ constexpr int kStaticSmemReserve = 2048;  // barriers, warp sums, flag, slack
 
 using KernelFn = void (*)(Params);
 
-// Kernel instances. VPT = 2 (8 KiB copies) serves N <= 8, with a compile-time
-// N for 1, 2, 4 and 8; VPT = 1 (4 KiB copies) serves N = 9..16, whose stages
-// would not fit three deep at 8 KiB, with a compile-time N for 16. Every
-// shape exists in a general and an EXACT (whole-chunk rows) form.
-#define TW_V2(K, E) {fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 1, E>, fused_kernel<K, 2, 2, E>, \
-                     fused_kernel<K, 2, 4, E>, fused_kernel<K, 2, 8, E>}
-const KernelFn kVpt2[2][4][5] = {
-    {TW_V2(2, false), TW_V2(4, false), TW_V2(8, false), TW_V2(16, false)},
-    {TW_V2(2, true), TW_V2(4, true), TW_V2(8, true), TW_V2(16, true)}};
-#undef TW_V2
+// Kernel instances. VPT = 2 (8 KiB copies) serves N <= 8 with a compile-time
+// N for every N at H <= 8192 (KMAX 2 and 4) and for 1, 2, 4, 8 at larger H;
+// VPT = 1 (4 KiB copies) serves N = 9..16, whose stages would not fit three
+// deep at 8 KiB, with a compile-time N for 16. Other shapes use a runtime-N
+// instance. Every shape exists in a general and an EXACT (whole-chunk rows)
+// form. Columns of kVpt2: N = runtime, 1, 2, 4, 8, 3, 5, 6, 7.
+#define TW_V2S(K, E) {fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 1, E>, fused_kernel<K, 2, 2, E>, \
+                      fused_kernel<K, 2, 4, E>, fused_kernel<K, 2, 8, E>, fused_kernel<K, 2, 3, E>, \
+                      fused_kernel<K, 2, 5, E>, fused_kernel<K, 2, 6, E>, fused_kernel<K, 2, 7, E>}
+#define TW_V2L(K, E) {fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 1, E>, fused_kernel<K, 2, 2, E>, \
+                      fused_kernel<K, 2, 4, E>, fused_kernel<K, 2, 8, E>, fused_kernel<K, 2, 0, E>, \
+                      fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 0, E>}
+const KernelFn kVpt2[2][4][9] = {
+    {TW_V2S(2, false), TW_V2S(4, false), TW_V2L(8, false), TW_V2L(16, false)},
+    {TW_V2S(2, true), TW_V2S(4, true), TW_V2L(8, true), TW_V2L(16, true)}};
+#undef TW_V2S
+#undef TW_V2L
 #define TW_V1(K, E) {fused_kernel<K, 1, 0, E>, fused_kernel<K, 1, 16, E>}
 const KernelFn kVpt1[2][5][2] = {
     {TW_V1(1, false), TW_V1(2, false), TW_V1(4, false), TW_V1(8, false), TW_V1(16, false)},
     {TW_V1(1, true), TW_V1(2, true), TW_V1(4, true), TW_V1(8, true), TW_V1(16, true)}};
 #undef TW_V1
-constexpr int kNumKernels = 40 + 20;
+constexpr int kNumKernels = 72 + 20;
 
 // Per-device attributes, queried once; the launch path reads them without a
 // lock once `ready` is set (the flags live in static storage, so they start
@@ -542,7 +549,19 @@ int log2_pow2_at_least(int x) {
 }
 
 // Column of the instance tables for N (0: runtime N).
-int partials_index_vpt2(int n) { return n == 1 ? 1 : n == 2 ? 2 : n == 4 ? 3 : n == 8 ? 4 : 0; }
+int partials_index_vpt2(int n) {
+  switch (n) {
+    case 1: return 1;
+    case 2: return 2;
+    case 4: return 3;
+    case 8: return 4;
+    case 3: return 5;
+    case 5: return 6;
+    case 6: return 7;
+    case 7: return 8;
+    default: return 0;
+  }
+}
 int partials_index_vpt1(int n) { return n == 16 ? 1 : 0; }
 
 int vpt_for(int n) { return n <= 8 ? 2 : 1; }
@@ -556,11 +575,11 @@ void select_kernel(int vpr, int n, int* index, KernelFn* fn, int* kmax) {
   const int exact = vpr == (1 << k) * kSlotVec ? 1 : 0;
   if (vpt == 2) {
     const int ki = k - 1, ni = partials_index_vpt2(n);  // KMAX 2..16
-    *index = exact * 20 + ki * 5 + ni;
+    *index = exact * 36 + ki * 9 + ni;
     *fn = kVpt2[exact][ki][ni];
   } else {
     const int ni = partials_index_vpt1(n);  // KMAX 1..16
-    *index = 40 + exact * 10 + k * 2 + ni;
+    *index = 72 + exact * 10 + k * 2 + ni;
     *fn = kVpt1[exact][k][ni];
   }
 }
