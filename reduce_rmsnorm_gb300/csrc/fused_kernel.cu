@@ -26,9 +26,10 @@
 //     combine of the 8 warp sums, rsqrtf, and Y = (z * r) * gamma stored with
 //     16-byte stores. The per-row arithmetic depends only on H, so every grid
 //     size (SM budget), split and shard gives bitwise the same rows.
-//   * L2 policy per call: evict-first loads and a streaming output for N <= 2
-//     or N >= 9 with an output of at most an eighth of the L2, and for N <= 2
-//     with an output of at least 7/16 of it; otherwise the normal policy.
+//   * L2 policy per call: evict-first loads and a streaming output when no
+//     CTA owns more than one row, for N <= 2 or N >= 9 with an output of at
+//     most an eighth of the L2, and for N <= 2 with an output of at least
+//     7/16 of it; otherwise the normal policy.
 //   * Programmatic dependent launch: the CTAs set up their barriers while the
 //     previous kernel in the stream drains, ask L2 for the first ~144 KiB of
 //     their rows (a prefetch hint, when a CTA owns more than one row), then
@@ -650,22 +651,28 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
   p.residual = static_cast<uint4*>(a.residual);
   p.out = static_cast<uint4*>(a.out);
   p.smid_out = smid_out;
-  // L2 policy per call, measured with the prefetch below in place (back to
-  // back, interleaved, on three GB300s): normal loads win for N = 3..8 at
-  // every size (+1-6% at T = 512-4096, H = 4096-16384). Evict-first loads
-  // with a streaming output win for N <= 2 and N >= 9 while the output is at
-  // most an eighth of the L2 (+1-6% at T <= 1024, H = 8192), and for N <= 2
-  // again once the output reaches 7/16 of the L2 (+1-3.5% at T = 4096-8192);
-  // in between, normal loads win by 2-5%.
+  // L2 policy per call, measured back to back, interleaved, on three GB300s.
+  // With the prefetch below in place (some CTA owns more than one row),
+  // normal loads win for N = 3..8 at every size (+1-6% at T = 384-4096,
+  // H = 4096-16384). Evict-first loads with a streaming output win for
+  // N <= 2 and N >= 9 while the output is at most an eighth of the L2 (+1-6%
+  // at T <= 1024, H = 8192), and for N <= 2 again once the output reaches
+  // 7/16 of the L2 (+1-3.5% at T = 4096-8192); in between, normal loads win
+  // by 2-5%. Without the prefetch (one row per CTA) evict-first wins for
+  // every N (+1-6% at T = 32-128).
   const int64_t out_bytes = a.rows * a.hidden * 2;
   const int64_t l2 = static_cast<int64_t>(d->l2_bytes);
   const bool small_out = out_bytes * 8 <= l2;
   const bool large_out = out_bytes * 16 >= l2 * 7;
-  p.l2_stream = ((a.n <= 2 && (small_out || large_out)) || (a.n >= 9 && small_out)) ? 1 : 0;
+  const bool one_row_per_cta = a.rows <= shape.grid;
+  p.l2_stream = (one_row_per_cta || (a.n <= 2 && (small_out || large_out)) ||
+                 (a.n >= 9 && small_out))
+                    ? 1
+                    : 0;
   // About 144 KiB per CTA, shared among the N + 1 sources. Only when some CTA
   // owns more than one row: with one row per CTA no CTA starts early.
-  p.prefetch_bytes = a.rows > shape.grid ? (kPrefetchPerCta / static_cast<uint32_t>(a.n + 1)) & ~15u
-                                         : 0u;
+  p.prefetch_bytes = !one_row_per_cta ? (kPrefetchPerCta / static_cast<uint32_t>(a.n + 1)) & ~15u
+                                      : 0u;
   p.rows = a.rows;
   p.vec_per_row = static_cast<int>(a.hidden / 8);
   p.n_partials = a.n;
