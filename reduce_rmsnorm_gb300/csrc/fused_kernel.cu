@@ -659,7 +659,8 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
   // at T <= 1024, H = 8192), and for N <= 2 again once the output reaches
   // 7/16 of the L2 (+1-3.5% at T = 4096-8192); in between, normal loads win
   // by 2-5%. Without the prefetch (one row per CTA) evict-first wins for
-  // every N (+1-6% at T = 32-128).
+  // N = 4 and 8 at every shape measured (+2-10% at T = 32-152,
+  // H = 4096-16384).
   const int64_t out_bytes = a.rows * a.hidden * 2;
   const int64_t l2 = static_cast<int64_t>(d->l2_bytes);
   const bool small_out = out_bytes * 8 <= l2;
