@@ -230,13 +230,20 @@ def tw_fused_reduce_residual_rmsnorm(partials, residual, gamma, eps, out, stream
 
 
 def tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=None, sm_budget=0):
-    """The fused call that also records each CTA's SM id into ``smid_out`` (int32)."""
+    """The fused call that also records each CTA's SM id into ``smid_out``: a
+    contiguous int32 CUDA tensor with at least the launch grid's length
+    (``tw_launch_shape(T, H, N, sm_budget)["grid"]``). The kernel writes one
+    entry per CTA, so a shorter buffer is refused here, before any launch."""
+    import torch
     arr, n, T, H = _step_args(partials, residual, gamma, out)
+    grid = tw_launch_shape(T, H, n, sm_budget)["grid"] if T > 0 else 0
+    if not (isinstance(smid_out, torch.Tensor) and smid_out.dtype is torch.int32 and
+            smid_out.is_cuda and smid_out.is_contiguous() and smid_out.numel() >= grid):
+        raise ValueError("smid_out must be a contiguous int32 CUDA tensor with at least %d "
+                         "entries (the launch grid)" % grid)
     st = lib().tw_fused_debug_smid(arr, n, _ptr(residual), _ptr(gamma), float(eps), T, H, _ptr(out),
                                    _stream(stream), int(sm_budget), _ptr(smid_out))
     _check(st, "tw_fused_debug_smid")
-
-
 
 
 def _opts_arg(offsets, min_split_tokens):

@@ -204,6 +204,25 @@ def test_binding_rejects_wrong_dtype_shape_or_strides():
     assert_same(R, to_gpu(p, r, g)[1])                                        # nothing ran
 
 
+def test_binding_rejects_a_short_or_mistyped_smid_buffer():
+    """The debug call writes one int32 per CTA: the binding refuses a buffer
+    shorter than the grid, or of another dtype, before any launch."""
+    p, r, g = synth.make_inputs(300, 4096, 2, 0.02, seed=4)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    grid = tw.tw_launch_shape(300, 4096, 2, 0)["grid"]
+    for bad in (torch.empty(grid - 1, dtype=torch.int32, device="cuda"),
+                torch.empty(grid, dtype=torch.int64, device="cuda"),
+                torch.empty(grid, dtype=torch.int32)):
+        with pytest.raises(ValueError, match="smid_out"):
+            tw.tw_fused_debug_smid(P, R, G, EPS, out, bad)
+    assert_same(R, to_gpu(p, r, g)[1])                                        # nothing ran
+    smid = torch.full((grid,), -1, dtype=torch.int32, device="cuda")
+    tw.tw_fused_debug_smid(P, R, G, EPS, out, smid)
+    torch.cuda.synchronize()
+    assert min(smid.cpu().tolist()) >= 0
+
+
 def test_misaligned_pointer_rejected_on_device_tensors():
     p, r, g = synth.make_inputs(4, 4096, 2, 0.02)
     P, R, G = to_gpu(p, r, g)
