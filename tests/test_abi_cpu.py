@@ -111,6 +111,25 @@ def test_planner_random_default_grid(L):
             oplanner.wave_split(T, C, S, tw.DEFAULT_OFFSETS, mins), (T, C, S, mins)
 
 
+def test_planner_on_the_projection_cta_formula(L):
+    """The C planner equals the brute-force oracle on the CTA counts of the
+    row-parallel projection, C = ceil(T/128) * (H/128) / 8: every token count
+    1024..9600 at H = 8192 on 148 SMs, and for H = 4096, 8192, 16384 on 132,
+    144, 148 and 152 SMs every count 1024..2048 plus a stride-37 sweep to
+    9600. The plans taken must use every offset of the default grid."""
+    cases = [(T, 8192, 148) for T in range(1024, 9601)]
+    cases += [(T, H, S) for H in (4096, 8192, 16384) for S in (132, 144, 148, 152)
+              for T in list(range(1024, 2049)) + list(range(2049, 9601, 37))]
+    used = set()
+    for T, H, S in cases:
+        C = math.ceil(T / 128) * (H // 128) // 8
+        want = oplanner.wave_split(T, C, S)
+        assert tw.tw_wave_split(T, C, S) == want, (T, H, S)
+        if want[1] > 0:
+            used.add(abs(want[0] - T // 2))
+    assert used == set(tw.DEFAULT_OFFSETS), sorted(used)
+
+
 def test_planner_custom_offsets_unsorted_duplicates(L):
     rng = np.random.Generator(np.random.PCG64(99))
     for _ in range(200):
