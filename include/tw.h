@@ -86,7 +86,9 @@ typedef enum {
  *   N          1 .. TW_MAX_PARTIALS.
  *   residual   device bf16 [T, H], read then overwritten with bf16(z).
  *   gamma      device bf16 [H], read only.
- *   eps        >= 0 and finite (1e-5 for the Llama workloads).
+ *   eps        >= 0 and finite (1e-5 for the Llama workloads). With eps = 0
+ *              a row whose z is all zero has no scale (0 * rsqrt(0)): its
+ *              out row is NaN, as the formula gives; with eps > 0 it is 0.
  *   T          token rows, >= 0; T == 0 is a no-op returning TW_OK.
  *   H          hidden size, 8 .. TW_MAX_HIDDEN, a multiple of 8.
  *   out        device bf16 [T, H], written. It may be exactly the buffer of

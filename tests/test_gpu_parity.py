@@ -122,6 +122,21 @@ def test_zero_and_constant_rows():
     assert torch.allclose(o[2], want.to(torch.bfloat16).float(), rtol=2 ** -7, atol=0)
 
 
+def test_eps_zero_rows_and_the_zero_row():
+    """eps = 0 (allowed: eps >= 0). Non-zero rows follow the formula with no
+    eps; a row whose z is all zero has no scale, 0 * rsqrt(0), so its Y is
+    NaN in every element, as in the formula, while its updated residual is 0."""
+    T, H, N = 5, 4096, 2
+    p, r, g = synth.make_inputs(T, H, N, 0.02, seed=10)
+    p[:, 3] = 0
+    r[3] = 0
+    R, out = run(p, r, g, eps=0.0)
+    keep = [0, 1, 2, 4]
+    check_rows(p, r, g, 0.0, R, out, rows=keep)
+    assert torch.all(R[3] == 0)
+    assert torch.all(torch.isnan(out[3].float()))
+
+
 def test_subnormal_inputs_are_not_flushed():
     """bf16 subnormals (|x| < 2^-126) in partials and residual: the fp32 sums
     must keep them (no flush to zero), so the updated residual stays bit-exact
