@@ -88,62 +88,184 @@ def ctas_unsplit(T, H):
     return math.ceil(T / 128) * (H // 128) // 8
 
 
-class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
-
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index, period_ms=50):
-        self.proc = None
+
+class NvmlSource:
+    """Read-only NVML device queries (libnvidia-ml, which ships with the
+    driver) through ctypes: SM clock, maximum SM clock, power draw and the
+    active clock-event reasons. Nothing is set."""
+
+    CLOCK_SM = 1
+    REASON_BITS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"),
+                   (0x20, "sw_thermal_slowdown"), (0x40, "hw_thermal_slowdown"))
+    name = "nvml"
+
+    def __init__(self, uuid, index):
+        import ctypes
+        self.ct = ctypes
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        h = ctypes.c_void_p()
+        by_uuid = bool(uuid) and L.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+        if not by_uuid and L.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+            L.nvmlShutdown()
+            raise OSError("no NVML handle for the device")
+        self.L, self.h = L, h
+        self.reasons_fn = (getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or
+                           getattr(L, "nvmlDeviceGetCurrentClocksThrottleReasons", None))
+
+    def sample(self):
+        ct, L, h = self.ct, self.L, self.h
+        clk, mx, mw, bits = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if (L.nvmlDeviceGetClockInfo(h, self.CLOCK_SM, ct.byref(clk)) != 0 or
+                L.nvmlDeviceGetMaxClockInfo(h, self.CLOCK_SM, ct.byref(mx)) != 0):
+            return None
+        power = mw.value / 1000.0 if L.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else 0.0
+        reasons = []
+        if self.reasons_fn is not None and self.reasons_fn(h, ct.byref(bits)) == 0:
+            reasons = [name for bit, name in self.REASON_BITS if bits.value & bit]
+        return {"sm": float(clk.value), "max": float(mx.value), "power": power,
+                "reasons": reasons}
+
+    def close(self):
+        self.L.nvmlShutdown()
+
+
+class SmiSource:
+    """One `nvidia-smi --query-gpu` call per sample (used where NVML cannot
+    be loaded)."""
+
+    name = "nvidia-smi"
+
+    def __init__(self, index):
+        self.index = index
+
+    def sample(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(device_index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.proc.stdout.readline()  # first sample: sampler is running
+            out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + SMI_FIELDS,
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                 timeout=10).stdout
         except Exception:
-            self.proc = None
+            return None
+        rows = [r for r in map(clock_row, out.splitlines()) if r]
+        return rows[0] if rows else None
+
+    def close(self):
+        pass
+
+
+class ClockSampler:
+    """SM clock, power and clock-event reasons sampled DURING a timed region.
+
+    Construct it before the warm-up, so that starting it does not leave the
+    GPU idle (and its clock falling) just before the region. A background
+    thread samples every period_ms. take_now() adds a sample from the
+    caller: taken right after the region's steps are enqueued, while the GPU
+    still runs them, it gives a region shorter than the period a sample from
+    inside it. begin() and end() mark the region on the host clock (end()
+    after the synchronise that closes it); stop() summarises the samples
+    taken between the marks."""
+
+    def __init__(self, source, period_ms=20):
+        import threading
+        self.source = source
+        self.samples = []
+        self.lock = threading.Lock()
+        self.t0 = self.t1 = None
+        self.halt = threading.Event()
+        self.period = period_ms / 1e3
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    @classmethod
+    def for_device(cls, dev, index):
+        """NVML for torch device `dev` (matched by UUID, else NVML index
+        `index`), else nvidia-smi; None if neither works."""
+        import torch
+        try:
+            uuid = str(torch.cuda.get_device_properties(dev).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            uuid = None
+        for make in (lambda: NvmlSource(uuid, index), lambda: SmiSource(index)):
+            try:
+                src = make()
+                if src.sample() is not None:
+                    return cls(src)
+            except Exception:
+                continue
+        return None
+
+    def _take(self):
+        t = time.perf_counter()
+        r = self.source.sample()
+        if r is not None:
+            r["t"] = t
+            with self.lock:
+                self.samples.append(r)
+
+    def _loop(self):
+        while not self.halt.wait(self.period):
+            self._take()
+
+    def take_now(self):
+        self._take()
+
+    def begin(self):
+        self.t0 = time.perf_counter()
+
+    def end(self):
+        self.t1 = time.perf_counter()
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        return parse_clock_lines(out.splitlines())
+        self.halt.set()
+        self.thread.join(timeout=10)
+        self.source.close()
+        with self.lock:
+            rows = [r for r in self.samples if self.t0 is not None and self.t1 is not None and
+                    self.t0 <= r["t"] <= self.t1]
+        out = summarise_clocks(rows)
+        if out is not None:
+            out["source"] = self.source.name
+            out["window"] = "timed region (%.1f ms)" % ((self.t1 - self.t0) * 1e3)
+        return out
 
 
-def parse_clock_lines(lines):
-    """Summarise `nvidia-smi --query-gpu=<ClockSampler.FIELDS> --format=csv,noheader,nounits`
-    lines: median SM clock, max clock, max power, and the throttle reasons seen
-    active in any sample. None if no line parses."""
-    rows = []
-    for line in lines:
-        f = [x.strip() for x in line.split(",")]
-        if len(f) < 9:
-            continue
-        try:
-            rows.append(dict(sm=float(f[1]), max=float(f[2]), power=float(f[3]),
-                             hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
-        except ValueError:
-            continue
+def clock_row(line):
+    """One `nvidia-smi --query-gpu=<SMI_FIELDS> --format=csv,noheader,nounits`
+    line as a sample dict, or None."""
+    f = [x.strip() for x in line.split(",")]
+    if len(f) < 9:
+        return None
+    try:
+        row = dict(sm=float(f[1]), max=float(f[2]), power=float(f[3]))
+    except ValueError:
+        return None
+    row["reasons"] = [name for k, name in ((5, "hw_slowdown"), (6, "hw_thermal_slowdown"),
+                                           (7, "sw_thermal_slowdown"), (8, "sw_power_cap"))
+                      if f[k].lower().startswith("active")]
+    return row
+
+
+def summarise_clocks(rows):
+    """Median SM clock, max clock, max power, and the clock-event reasons seen
+    active in any sample; None without samples."""
     if not rows:
         return None
-    reasons = set()
-    for r in rows:
-        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
-                          ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
-            if r[key].lower().startswith("active"):
-                reasons.add(name)
     return {"sm_mhz": statistics.median(r["sm"] for r in rows),
             "sm_max_mhz": max(r["max"] for r in rows),
             "power_w_max": max(r["power"] for r in rows),
-            "samples": len(rows), "reasons": sorted(reasons)}
+            "samples": len(rows),
+            "reasons": sorted({name for r in rows for name in r["reasons"]})}
+
+
+def parse_clock_lines(lines):
+    """Summary of nvidia-smi sample lines (see clock_row)."""
+    return summarise_clocks([r for r in map(clock_row, lines) if r])
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -254,6 +376,8 @@ def gpu_arm(args, rank, world):
         g.replay()
 
     step = step_graph if args.mode == "graph" else step_eager
+    # started before the warm-up: starting it later would idle the GPU
+    clocks = ClockSampler.for_device(dev, local) if rank == 0 else None
     sa.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(sa):
         for k in range(max(args.warmup, len(calls))):
@@ -265,17 +389,22 @@ def gpu_arm(args, rank, world):
     launches_per_step = (1 if prefix > 0 else 0) + (1 if suffix > 0 else 0)
 
     # timed region: K steps back to back, events on the launching stream only
-    clocks = ClockSampler(local) if rank == 0 else None
     barrier(world)
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.begin()
     with torch.cuda.stream(sa):
         t_start.record(sa)
         for k in range(args.steps):
             step(args.warmup + k)
         t_end.record(sa)
+    if clocks and not t_end.query():
+        clocks.take_now()  # the GPU is still running the timed steps
     torch.cuda.synchronize()
+    if clocks:
+        clocks.end()
     barrier(world)
     clk = clocks.stop() if clocks else None
     elapsed_ms = t_start.elapsed_time(t_end)

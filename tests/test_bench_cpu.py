@@ -46,6 +46,38 @@ def test_clock_lines_summary():
     assert bench.parse_clock_lines([]) is None
 
 
+def test_clock_sampler_keeps_only_the_timed_region():
+    """Samples from before begin() (the warm-up) and after end() are dropped;
+    take_now() gives a short region its own sample."""
+    clocks = iter([1400.0, 1500.0, 2070.0, 2055.0, 900.0])
+
+    class Fake:
+        name = "fake"
+
+        def sample(self):
+            return {"sm": next(clocks, 900.0), "max": 2070.0, "power": 500.0,
+                    "reasons": ["sw_power_cap"]}
+
+        def close(self):
+            pass
+
+    s = bench.ClockSampler(Fake(), period_ms=10 ** 6)   # the thread never fires
+    s.take_now()
+    s.take_now()                                      # warm-up: 1400, 1500
+    s.begin()
+    s.take_now()
+    s.take_now()                                      # region: 2070, 2055
+    s.end()
+    s.take_now()                                      # after: 900
+    c = s.stop()
+    assert c["samples"] == 2 and c["sm_mhz"] == 2062.5 and c["reasons"] == ["sw_power_cap"]
+    assert c["source"] == "fake" and c["window"].startswith("timed region")
+    empty = bench.ClockSampler(Fake(), period_ms=10 ** 6)
+    empty.begin()
+    empty.end()
+    assert empty.stop() is None
+
+
 def test_cta_model_of_the_split_workload():
     # ceil(T/128) * (H/128) / 8: the configs' 64 / 128 / 256 / 512 CTAs
     assert [bench.ctas_unsplit(T, 8192) for T in (1024, 2048, 4096, 8192)] == [64, 128, 256, 512]
