@@ -12,7 +12,8 @@
  *     rows of H hidden values, row stride H elements. A shard or half of a
  *     tensor is passed by offsetting its pointers by row0 * H elements.
  *   - The caller owns every buffer. libtw allocates no device memory; it keeps
- *     only per-device launch attributes (SM count, shared-memory limit).
+ *     only per-device launch attributes (SM count, shared-memory limit, L2
+ *     size, which sets the per-call L2 policy).
  *   - Launches are asynchronous on the stream(s) given; a device fault shows
  *     at the caller's next synchronisation, as usual in CUDA. Work runs on the
  *     device that is current on the calling thread.
