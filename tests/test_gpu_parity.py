@@ -88,20 +88,27 @@ def test_parity_llama70b_all_rows():
     p, r, g = synth.make_workload("llama70b_t1024_h8192_n8")
     P, R, G = to_gpu(p, r, g)
     out = torch.empty_like(R)
-    C = math.ceil(1024 / 128) * 8
-    prefix, _ = tw.tw_wave_split(1024, C, 148)
-    s2 = torch.cuda.Stream()
-    tw.tw_run_split(prefix, P, R, G, EPS, out, torch.cuda.current_stream(), s2)
+    C = math.ceil(1024 / 128) * (8192 // 128) // 8
+    step = tw.PlannedSplitCall(C, 148, P, R, G, EPS, out, torch.cuda.current_stream(),
+                               torch.cuda.Stream())
+    assert step() == (1024, 0)                 # one wave of 64 CTAs: the batch stays whole
     torch.cuda.synchronize()
     stats = check_rows(p, r, g, EPS, R, out)
     assert stats["max_ulp"] <= 2.0
 
 
 def test_parity_llama405b_sampled_rows():
-    """T=8192, H=16384, N=8 with 1% outliers x50: full-size launch, 256 seeded
-    random rows plus the first and last checked against the oracle."""
+    """T=8192, H=16384, N=8 with 1% outliers x50: the benchmark's planned call
+    at full size, 256 seeded random rows plus the first and last checked
+    against the oracle."""
     p, r, g = synth.make_workload("llama405b_t8192_h16384_n8")
-    R, out = run(p, r, g)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    C = math.ceil(8192 / 128) * (16384 // 128) // 8
+    step = tw.PlannedSplitCall(C, 148, P, R, G, EPS, out, torch.cuda.current_stream(),
+                               torch.cuda.Stream())
+    assert step() == (8192, 0)                 # no offset keeps 1024 CTAs within 7 waves
+    torch.cuda.synchronize()
     rng = np.random.Generator(np.random.PCG64(405))
     rows = np.unique(np.concatenate([[0, 8191], rng.choice(8192, 256, replace=False)]))
     check_rows(p, r, g, EPS, R, out, rows=rows)
