@@ -68,6 +68,31 @@ def test_parity_small(T, H, N, sig, outl):
     check_rows(p, r, g, EPS, R, out)
 
 
+def _one_case_per_instance():
+    """(H, N) pairs that reach every distinct kernel instance. The launch
+    picks VPT = 2 (8 KiB copies) for N <= 8 and VPT = 1 (4 KiB) above; KMAX
+    is the smallest power of two >= the row's chunks * VPT; a row is EXACT
+    when H / 8 == KMAX * 256. For each KMAX an exact H and a ragged H of the
+    same KMAX are paired with every N of the compile-time instances and with
+    N that take the runtime-N instance."""
+    cases = []
+    for exact, ragged in ((4096, 2056), (8192, 6152), (16384, 12296), (32768, 24584)):
+        for n in range(1, 9):
+            cases += [(exact, n), (ragged, n)]
+    for exact, ragged in ((2048, 1032), (4096, 3080), (8192, 6152), (16384, 12296),
+                          (32768, 24584)):
+        for n in (9, 15, 16):
+            cases += [(exact, n), (ragged, n)]
+    return cases
+
+
+@pytest.mark.parametrize("H,N", _one_case_per_instance())
+def test_parity_every_kernel_instance(H, N):
+    p, r, g = synth.make_inputs(3, H, N, 0.02, seed=H + N)
+    R, out = run(p, r, g)
+    check_rows(p, r, g, EPS, R, out)
+
+
 @pytest.mark.parametrize("eps", [0.0, 1e-6, 1e-5, 0.5])
 def test_parity_eps(eps):
     p, r, g = synth.make_inputs(17, 4096, 4, 0.02, seed=5)
