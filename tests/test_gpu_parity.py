@@ -86,10 +86,13 @@ def _one_case_per_instance():
     return cases
 
 
+@pytest.mark.parametrize("T,budget", [(3, 0), (40, 3)])
 @pytest.mark.parametrize("H,N", _one_case_per_instance())
-def test_parity_every_kernel_instance(H, N):
-    p, r, g = synth.make_inputs(3, H, N, 0.02, seed=H + N)
-    R, out = run(p, r, g)
+def test_parity_every_kernel_instance(H, N, T, budget):
+    """T=3: one row per CTA (no L2 prefetch); T=40 on 3 SMs: 13-14 rows per
+    CTA, so the ring wraps across rows and the prefetch is issued."""
+    p, r, g = synth.make_inputs(T, H, N, 0.02, seed=H + N + T)
+    R, out = run(p, r, g, sm_budget=budget)
     check_rows(p, r, g, EPS, R, out)
 
 
