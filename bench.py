@@ -194,10 +194,14 @@ class ClockSampler:
         for make in (lambda: NvmlSource(uuid, index), lambda: SmiSource(index)):
             try:
                 src = make()
+            except Exception:
+                continue
+            try:
                 if src.sample() is not None:
                     return cls(src)
             except Exception:
-                continue
+                pass
+            src.close()
         return None
 
     def _take(self):
