@@ -78,6 +78,58 @@ def test_clock_sampler_keeps_only_the_timed_region():
     assert empty.stop() is None
 
 
+def test_nvml_source_reads_through_a_fake_library(monkeypatch):
+    """NvmlSource against a fake libnvidia-ml: handle by UUID, SM clock and
+    maximum in MHz, power in mW -> W, and the clock-event reason bits mapped
+    to names (0x4 power cap, 0x8 hardware slowdown, 0x20 software thermal,
+    0x40 hardware thermal); idle (0x1) is not a reason to report. Only read
+    calls exist in the fake, so any attempt to set something would fail."""
+    import ctypes
+    calls = []
+
+    def out(arg, value):
+        arg._obj.value = value
+        return 0
+
+    class FakeNvml:
+        def nvmlInit_v2(self):
+            calls.append("init")
+            return 0
+
+        def nvmlShutdown(self):
+            calls.append("shutdown")
+            return 0
+
+        def nvmlDeviceGetHandleByUUID(self, uuid, handle):
+            calls.append(uuid)
+            return out(handle, 1234) if uuid == b"GPU-abc" else 999
+
+        def nvmlDeviceGetHandleByIndex_v2(self, index, handle):
+            return out(handle, 99)
+
+        def nvmlDeviceGetClockInfo(self, h, kind, v):
+            return out(v, 1965 if kind == 1 else 0)
+
+        def nvmlDeviceGetMaxClockInfo(self, h, kind, v):
+            return out(v, 2070)
+
+        def nvmlDeviceGetPowerUsage(self, h, v):
+            return out(v, 612345)
+
+        def nvmlDeviceGetCurrentClocksEventReasons(self, h, v):
+            return out(v, 0x1 | 0x4 | 0x40)
+
+    monkeypatch.setattr(ctypes, "CDLL", lambda name: FakeNvml())
+    src = bench.NvmlSource("GPU-abc", 0)
+    assert src.h.value == 1234
+    s = src.sample()
+    assert s == {"sm": 1965.0, "max": 2070.0, "power": 612.345,
+                 "reasons": ["sw_power_cap", "hw_thermal_slowdown"]}
+    src.close()
+    assert calls == ["init", b"GPU-abc", "shutdown"]
+    assert bench.NvmlSource("GPU-other", 3).h.value == 99   # falls back to the index
+
+
 def test_cta_model_of_the_split_workload():
     # ceil(T/128) * (H/128) / 8: the configs' 64 / 128 / 256 / 512 CTAs
     assert [bench.ctas_unsplit(T, 8192) for T in (1024, 2048, 4096, 8192)] == [64, 128, 256, 512]
