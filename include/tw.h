@@ -192,7 +192,10 @@ TW_API int tw_split_lookup(const int64_t* table_tokens, const int64_t* table_pre
  * work already queued on stream_a; on return stream_a is ordered after both
  * halves. An empty half is not launched. The result is bitwise the same as
  * the unsplit call. The fork and join use two CUDA events per device that
- * each calling host thread creates on first use and keeps; the call never
+ * each calling host thread takes on first use from a process-wide pool
+ * (created there when the pool is empty) and hands back to it when the
+ * thread exits; pooled events last until the process ends, so their number
+ * stays bounded by the most threads that called at once. The call never
  * creates or destroys streams. stream_a == stream_b is allowed (the halves
  * then run in order, with no events). The call can be captured into a CUDA
  * graph (the two streams become a fork and a join in the graph) once an

@@ -186,15 +186,43 @@ def _check_tensor(t, name, shape):
         raise _bad_tensor(t, name, shape)
 
 
-def _step_args(partials, residual, gamma, out):
+def _current_device():
+    """Index of the CUDA device current on this thread: the device the C ABI
+    launches on (it calls cudaGetDevice)."""
+    import torch
+    return torch.cuda.current_device()
+
+
+def _check_devices(where, tensors=(), streams=()):
+    """Every tensor and stream must be on the current device. The C ABI
+    launches on the current device and cannot tell from a raw pointer which
+    GPU owns it: another GPU's address would reach the kernel's bulk copies
+    and stores as a peer access, or fault. Streams given as raw handles
+    (ints) cannot be checked here."""
+    dev = _current_device()
+    for name, t in tensors:
+        if t is not None and t.device.index != dev:
+            raise ValueError("%s: %s is on %s but the current device is cuda:%d; all tensors "
+                             "and streams must be on the current device" % (where, name, t.device,
+                                                                            dev))
+    for name, s in streams:
+        d = getattr(s, "device", None)
+        if d is not None and d.index != dev:
+            raise ValueError("%s: %s is on %s but the current device is cuda:%d; all tensors "
+                             "and streams must be on the current device" % (where, name, d, dev))
+
+
+def _step_args(partials, residual, gamma, out, where="fused step", streams=()):
     """Validated (pointer array, N, T, H) for a fused step's tensors. An
     [N, T, H] stack is checked once and its N pointers are computed from its
-    base address and stride."""
+    base address and stride. Every tensor and stream must be on the current
+    device (_check_devices)."""
     import torch
     T, H = _shape(residual)
     _check_tensor(residual, "residual", (T, H))
     _check_tensor(gamma, "gamma", (H,))
     _check_tensor(out, "out", (T, H))
+    named = [("residual", residual), ("gamma", gamma), ("out", out)]
     if isinstance(partials, torch.Tensor) and partials.dim() == 3:
         n = int(partials.shape[0])
         if not (partials.dtype is torch.bfloat16 and partials.is_cuda and
@@ -204,11 +232,13 @@ def _step_args(partials, residual, gamma, out):
                              "slices (got %s, %s, shape %s, strides %s)"
                              % (T, H, partials.dtype, partials.device, tuple(partials.shape),
                                 partials.stride()))
+        _check_devices(where, named + [("partials", partials)], streams)
         base, step = partials.data_ptr(), partials.stride(0) * 2
         return (_vp * max(n, 1))(*[base + i * step for i in range(n)]), n, T, H
     seq = [partials] if isinstance(partials, torch.Tensor) else list(partials)
     for r, t in enumerate(seq):
         _check_tensor(t, "partials[%d]" % r, (T, H))
+    _check_devices(where, named + [("partials[%d]" % r, t) for r, t in enumerate(seq)], streams)
     arr, n = _partials_array(seq)
     return arr, n, T, H
 
@@ -223,7 +253,8 @@ def tw_fused_reduce_residual_rmsnorm(partials, residual, gamma, eps, out, stream
     residual (in/out), out: bf16 [T, H]; gamma: bf16 [H]. Shapes are read from
     ``residual``; layout and error rules are those of the C call.
     """
-    arr, n, T, H = _step_args(partials, residual, gamma, out)
+    arr, n, T, H = _step_args(partials, residual, gamma, out, "tw_fused_reduce_residual_rmsnorm",
+                              [("stream", stream)])
     st = lib().tw_fused_reduce_residual_rmsnorm(arr, n, _ptr(residual), _ptr(gamma), float(eps), T,
                                                 H, _ptr(out), _stream(stream), int(sm_budget))
     _check(st, "tw_fused_reduce_residual_rmsnorm")
@@ -235,12 +266,14 @@ def tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=No
     (``tw_launch_shape(T, H, N, sm_budget)["grid"]``). The kernel writes one
     entry per CTA, so a shorter buffer is refused here, before any launch."""
     import torch
-    arr, n, T, H = _step_args(partials, residual, gamma, out)
+    arr, n, T, H = _step_args(partials, residual, gamma, out, "tw_fused_debug_smid",
+                              [("stream", stream)])
     grid = tw_launch_shape(T, H, n, sm_budget)["grid"] if T > 0 else 0
     if not (isinstance(smid_out, torch.Tensor) and smid_out.dtype is torch.int32 and
             smid_out.is_cuda and smid_out.is_contiguous() and smid_out.numel() >= grid):
         raise ValueError("smid_out must be a contiguous int32 CUDA tensor with at least %d "
                          "entries (the launch grid)" % grid)
+    _check_devices("tw_fused_debug_smid", [("smid_out", smid_out)])
     st = lib().tw_fused_debug_smid(arr, n, _ptr(residual), _ptr(gamma), float(eps), T, H, _ptr(out),
                                    _stream(stream), int(sm_budget), _ptr(smid_out))
     _check(st, "tw_fused_debug_smid")
@@ -298,7 +331,8 @@ def tw_split_lookup(table, num_tokens, ctas_unsplit, num_sms, offsets=DEFAULT_OF
 def tw_run_split(prefix_tokens, partials, residual, gamma, eps, out, stream_a=None, stream_b=None,
                  sm_budget=0):
     """Rows [0, prefix) on stream_a, [prefix, T) on stream_b; stream_a joins both."""
-    arr, n, T, H = _step_args(partials, residual, gamma, out)
+    arr, n, T, H = _step_args(partials, residual, gamma, out, "tw_run_split",
+                              [("stream_a", stream_a), ("stream_b", stream_b)])
     st = lib().tw_run_split(int(prefix_tokens), arr, n, _ptr(residual), _ptr(gamma), float(eps), T,
                             H, _ptr(out), _stream(stream_a), _stream(stream_b), int(sm_budget))
     _check(st, "tw_run_split")
@@ -309,7 +343,8 @@ def tw_run_wave_split(ctas_unsplit, num_sms, partials, residual, gamma, eps, out
                       min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
     """The wave-aware plan and the split step in one C call; returns the plan
     (prefix_tokens, suffix_tokens)."""
-    arr, n, T, H = _step_args(partials, residual, gamma, out)
+    arr, n, T, H = _step_args(partials, residual, gamma, out, "tw_run_wave_split",
+                              [("stream_a", stream_a), ("stream_b", stream_b)])
     optp, keep = _opts_arg(offsets, min_split_tokens)
     p, s = _i64(), _i64()
     st = lib().tw_run_wave_split(int(ctas_unsplit), int(num_sms), optp, arr, n,
@@ -330,7 +365,8 @@ def tw_run_split_after(prefix_tokens, partials, residual, gamma, eps, out, strea
     """On `stream`: wait prefix_ready, fused step on rows [0, prefix); wait
     suffix_ready, fused step on rows [prefix, T). Events: torch.cuda.Event or
     raw cudaEvent_t handles."""
-    arr, n, T, H = _step_args(partials, residual, gamma, out)
+    arr, n, T, H = _step_args(partials, residual, gamma, out, "tw_run_split_after",
+                              [("stream", stream)])
     st = lib().tw_run_split_after(int(prefix_tokens), arr, n, _ptr(residual), _ptr(gamma),
                                   float(eps), T, H, _ptr(out), _stream(stream),
                                   _event(prefix_ready), _event(suffix_ready), int(sm_budget))
@@ -345,6 +381,8 @@ def tw_reduce_partials(partials, sum_out, stream=None):
         partials.dim() == 3 else list(partials)
     for r, t in enumerate(seq):
         _check_tensor(t, "partials[%d]" % r, (T, H))
+    _check_devices("tw_reduce_partials", [("sum_out", sum_out)] +
+                   [("partials[%d]" % r, t) for r, t in enumerate(seq)], [("stream", stream)])
     arr, n = _partials_array(seq)
     st = lib().tw_reduce_partials(arr, n, T, H, _ptr(sum_out), _stream(stream))
     _check(st, "tw_reduce_partials")
@@ -356,6 +394,8 @@ def tw_add_rmsnorm(sum_in, residual, gamma, eps, out, stream=None):
     for name, t, shape in (("sum_in", sum_in, (T, H)), ("residual", residual, (T, H)),
                            ("gamma", gamma, (H,)), ("out", out, (T, H))):
         _check_tensor(t, name, shape)
+    _check_devices("tw_add_rmsnorm", [("sum_in", sum_in), ("residual", residual),
+                                      ("gamma", gamma), ("out", out)], [("stream", stream)])
     st = lib().tw_add_rmsnorm(_ptr(sum_in), _ptr(residual), _ptr(gamma), float(eps), T, H,
                               _ptr(out), _stream(stream))
     _check(st, "tw_add_rmsnorm")
@@ -368,7 +408,7 @@ class FusedCall:
     the stream resolved at construction."""
 
     def __init__(self, partials, residual, gamma, eps, out, stream=None, sm_budget=0):
-        arr, n, T, H = _step_args(partials, residual, gamma, out)
+        arr, n, T, H = _step_args(partials, residual, gamma, out, "FusedCall", [("stream", stream)])
         self.tensors = (partials, residual, gamma, out)
         self._fn = lib().tw_fused_reduce_residual_rmsnorm
         self._args = (arr, _int(n), _ptr(residual), _ptr(gamma), ctypes.c_float(eps), _i64(T),
@@ -407,7 +447,8 @@ class SplitCall:
 
     def __init__(self, partials, residual, gamma, eps, out, stream_a=None, stream_b=None,
                  sm_budget=0):
-        arr, n, T, H = _step_args(partials, residual, gamma, out)
+        arr, n, T, H = _step_args(partials, residual, gamma, out, "SplitCall",
+                                  [("stream_a", stream_a), ("stream_b", stream_b)])
         self.tokens = T
         self.tensors = (partials, residual, gamma, out)
         self._fn = lib().tw_run_split
@@ -429,7 +470,8 @@ class PlannedSplitCall:
     def __init__(self, ctas_unsplit, num_sms, partials, residual, gamma, eps, out,
                  stream_a=None, stream_b=None, sm_budget=0, offsets=DEFAULT_OFFSETS,
                  min_split_tokens=DEFAULT_MIN_SPLIT_TOKENS):
-        arr, n, T, H = _step_args(partials, residual, gamma, out)
+        arr, n, T, H = _step_args(partials, residual, gamma, out, "PlannedSplitCall",
+                                  [("stream_a", stream_a), ("stream_b", stream_b)])
         self.tokens = T
         self.tensors = (partials, residual, gamma, out)
         optp, self._keep = _opts_arg(offsets, min_split_tokens)
@@ -453,7 +495,8 @@ class UnfusedCall:
     ``out`` in place (two launches)."""
 
     def __init__(self, partials, residual, gamma, eps, out, stream=None):
-        arr, n, T, H = _step_args(partials, residual, gamma, out)
+        arr, n, T, H = _step_args(partials, residual, gamma, out, "UnfusedCall",
+                                  [("stream", stream)])
         self.tensors = (partials, residual, gamma, out)
         L = lib()
         s = _stream(stream)

@@ -4,6 +4,8 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
+#include <vector>
 
 #include "tw.h"
 #include "tw_internal.h"
@@ -65,27 +67,64 @@ int validate(const void* const* partials, int N, void* residual, const void* gam
   return TW_OK;
 }
 
-// Two events per device for the split's fork and join, created on first use
-// by each host thread and kept for the thread's lifetime (an event is reused
-// only after the stream-wait that consumed its previous record was enqueued).
+// The split's fork and join events: one pair per (host thread, device), taken
+// from a process-wide pool on the thread's first split call on that device and
+// handed back to the pool when the thread exits. A pair is reused only after
+// the stream waits that consumed its previous records were enqueued, so reuse
+// keeps the ordering. Handing back makes no CUDA call (the context may already
+// be gone at thread or process exit); pooled events live until the process
+// ends, so their number is bounded by the most threads that ever called at
+// once, however many short-lived threads call over time.
 constexpr int kMaxDevices = 64;
-struct SplitEvents {
-  cudaEvent_t fork[kMaxDevices] = {};
-  cudaEvent_t join[kMaxDevices] = {};
+struct EventPair {
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join = nullptr;
 };
-thread_local SplitEvents t_events;
+struct EventPool {
+  std::mutex mutex;
+  std::vector<EventPair> free[kMaxDevices];
+};
+EventPool& event_pool() {
+  static EventPool* pool = new EventPool;  // never destroyed: used by thread-exit hand-backs
+  return *pool;
+}
+struct ThreadEvents {
+  EventPair pair[kMaxDevices];
+  ~ThreadEvents() {
+    EventPool& pool = event_pool();
+    std::lock_guard<std::mutex> lock(pool.mutex);
+    for (int d = 0; d < kMaxDevices; ++d)
+      if (pair[d].fork) pool.free[d].push_back(pair[d]);
+  }
+};
+thread_local ThreadEvents t_events;
 
 int split_events(cudaEvent_t* fork, cudaEvent_t* join) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TW_ERR_CUDA;
-  if (!t_events.fork[dev] &&
-      cudaEventCreateWithFlags(&t_events.fork[dev], cudaEventDisableTiming) != cudaSuccess)
-    return TW_ERR_CUDA;
-  if (!t_events.join[dev] &&
-      cudaEventCreateWithFlags(&t_events.join[dev], cudaEventDisableTiming) != cudaSuccess)
-    return TW_ERR_CUDA;
-  *fork = t_events.fork[dev];
-  *join = t_events.join[dev];
+  EventPair& mine = t_events.pair[dev];
+  if (!mine.fork) {
+    EventPair got;
+    {
+      EventPool& pool = event_pool();
+      std::lock_guard<std::mutex> lock(pool.mutex);
+      if (!pool.free[dev].empty()) {
+        got = pool.free[dev].back();
+        pool.free[dev].pop_back();
+      }
+    }
+    if (!got.fork) {
+      if (cudaEventCreateWithFlags(&got.fork, cudaEventDisableTiming) != cudaSuccess)
+        return TW_ERR_CUDA;
+      if (cudaEventCreateWithFlags(&got.join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventDestroy(got.fork);
+        return TW_ERR_CUDA;
+      }
+    }
+    mine = got;
+  }
+  *fork = mine.fork;
+  *join = mine.join;
   return TW_OK;
 }
 

@@ -395,9 +395,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
       if (++chunk == chunks) { chunk = 0; ++row; }
       if (++s == stages) { s = 0; round_parity ^= 1u; first_pass = false; }
     }
-    if (lane == 0 && *abort) {
-      // Let every copy this CTA issued land before the CTA exits: the last
-      // item issued on each stage completes after all earlier ones there.
+    if (lane == 0) {
+      // The producer owns the drain: every copy this CTA issued lands before
+      // the CTA can exit, whether or not a consumer gave up a wait (possibly
+      // after the producer left its loop). The last item issued on each stage
+      // completes after all earlier ones there. On the normal path the
+      // consumers have waited for (or will wait for) the same phases, so this
+      // returns as they complete.
       const long long last = issued - 1;
       for (int st = 0; st < stages && st <= last; ++st) {
         const long long it_last = last - ((last - st) % stages);

@@ -345,3 +345,77 @@ def test_binding_rejects_tensors_the_abi_cannot_describe():
                  lambda: tw.tw_add_rmsnorm(out, R, G, 1e-5, out)):
         with pytest.raises(ValueError, match="contiguous bf16 CUDA tensor"):
             call()
+
+
+class _FakeCudaTensor:
+    """Stands in for a bf16 CUDA tensor on a given device index: only the
+    attributes the binding reads before any library call."""
+
+    def __init__(self, shape, index, ptr=0x10000):
+        import torch
+        self.shape = torch.Size(shape)
+        self.dtype = torch.bfloat16
+        self.is_cuda = True
+        self.device = torch.device("cuda", index)
+        self._ptr = ptr
+
+    def is_contiguous(self):
+        return True
+
+    def dim(self):
+        return len(self.shape)
+
+    def data_ptr(self):
+        return self._ptr
+
+
+class _FakeStream:
+    def __init__(self, index):
+        import torch
+        self.device = torch.device("cuda", index)
+        self.cuda_stream = 0
+
+
+def test_binding_rejects_tensors_on_another_device(monkeypatch):
+    """The C ABI launches on the current device and cannot tell which GPU a
+    raw pointer belongs to, so the binding refuses any tensor or stream on
+    another device before a library call is made."""
+    monkeypatch.setattr(tw, "_current_device", lambda: 0)
+
+    def lib_must_not_be_called():
+        raise AssertionError("library called before the device check")
+
+    monkeypatch.setattr(tw, "lib", lib_must_not_be_called)
+    T, H = 4, 16
+
+    def inputs(bad):
+        dev = {name: 1 if name == bad else 0 for name in ("p0", "p1", "R", "G", "out")}
+        P = [_FakeCudaTensor((T, H), dev["p0"]), _FakeCudaTensor((T, H), dev["p1"])]
+        return (P, _FakeCudaTensor((T, H), dev["R"]), _FakeCudaTensor((H,), dev["G"]),
+                _FakeCudaTensor((T, H), dev["out"]))
+
+    for bad in ("p0", "p1", "R", "G", "out"):
+        P, R, G, out = inputs(bad)
+        for call in (lambda: tw.tw_fused_reduce_residual_rmsnorm(P, R, G, 1e-5, out),
+                     lambda: tw.tw_run_split(2, P, R, G, 1e-5, out),
+                     lambda: tw.tw_run_wave_split(8, 148, P, R, G, 1e-5, out),
+                     lambda: tw.tw_run_split_after(2, P, R, G, 1e-5, out),
+                     lambda: tw.FusedCall(P, R, G, 1e-5, out),
+                     lambda: tw.SplitCall(P, R, G, 1e-5, out),
+                     lambda: tw.PlannedSplitCall(8, 148, P, R, G, 1e-5, out),
+                     lambda: tw.UnfusedCall(P, R, G, 1e-5, out)):
+            with pytest.raises(ValueError, match="current device is cuda:0"):
+                call()
+    P, R, G, out = inputs(None)
+    with pytest.raises(ValueError, match="current device"):
+        tw.tw_reduce_partials([P[0], _FakeCudaTensor((T, H), 1)], out)
+    with pytest.raises(ValueError, match="current device"):
+        tw.tw_add_rmsnorm(_FakeCudaTensor((T, H), 1), R, G, 1e-5, out)
+    # streams on another device
+    for call in (lambda: tw.tw_fused_reduce_residual_rmsnorm(P, R, G, 1e-5, out,
+                                                             stream=_FakeStream(1)),
+                 lambda: tw.tw_run_split(2, P, R, G, 1e-5, out, _FakeStream(0), _FakeStream(1)),
+                 lambda: tw.SplitCall(P, R, G, 1e-5, out, _FakeStream(1), _FakeStream(0)),
+                 lambda: tw.tw_run_split_after(2, P, R, G, 1e-5, out, stream=_FakeStream(1))):
+        with pytest.raises(ValueError, match="stream"):
+            call()

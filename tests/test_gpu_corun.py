@@ -1,16 +1,20 @@
 """The split pipelined against a GEMM that produces partial 0 on another
 stream (tw_run_split_after): each fused half must start only after its GEMM
-half has finished. Checked by recomputing the unsplit fused step on the final
-partials and comparing bit for bit. Needs a GPU.
+half has finished. Checked two ways: against the oracle, on the final
+partials (partial 0 as the GEMM wrote it), the residual before the call and
+gamma, at the rows around the split and 64 seeded rows; and bit for bit
+against the unsplit fused step recomputed on the same partials. Needs a GPU.
 
 Pages: [G] "TokenWeave Guide: Compute-Communication Overlap for LLMs",
 "Architectural Foundations of TokenWeave"."""
 
+import numpy as np
 import pytest
 import torch
 
 import reduce_rmsnorm_gb300 as tw
 import synth
+from parity import check_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +29,8 @@ def _lib():
     assert tw.tw_device_status(reset=True) == 0
 
 
-@pytest.mark.parametrize("T,budget", [(4096, 4), (2048, 0), (1024, 8), (4864, 2)])
+@pytest.mark.parametrize("T,budget", [(4096, 4), (2048, 0), (1024, 8), (4864, 2), (4096, 0),
+                                      (1024, 2)])
 def test_split_after_gemm_matches_unsplit(T, budget):
     H, N, eps = 8192, 8, synth.EPS
     K = 4 * H // N
@@ -56,5 +61,10 @@ def test_split_after_gemm_matches_unsplit(T, budget):
     out_ref = torch.empty_like(R)
     tw.tw_fused_reduce_residual_rmsnorm(P, R0, G, eps, out_ref)
     torch.cuda.synchronize()
+    # against the oracle: the partials as the GEMM left them, the residual and
+    # gamma as they were before the call
+    rows = sorted({0, prefix - 1, prefix, T - 1} |
+                  set(np.random.default_rng(T + budget).choice(T, 64, replace=False).tolist()))
+    check_rows(P.cpu(), r, g, eps, R.cpu(), out.cpu(), rows=rows)
     assert torch.equal(R.view(torch.int16), R0.view(torch.int16))
     assert torch.equal(out.view(torch.int16), out_ref.view(torch.int16))
