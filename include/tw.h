@@ -245,6 +245,30 @@ TW_API int tw_run_split_after(int64_t prefix_tokens, const void* const* partials
                        tw_stream_t stream, tw_event_t prefix_ready, tw_event_t suffix_ready,
                        int sm_budget);
 
+/*
+ * tw_shard_rows -- the token-boundary shard of one rank, for the multi-GPU
+ * form of the step ([W] "Fix two: RMSNorm was never insignificant": the
+ * all-reduce is taken apart into a reduce-scatter and an all-gather at token
+ * boundaries, so that each rank normalises only its own whole token rows).
+ *
+ * With s = ceil(num_tokens / world), rank r owns rows
+ * [min(r * s, T), min((r + 1) * s, T)): shards are contiguous, disjoint, in
+ * rank order and cover every row exactly once; every shard has s rows except
+ * the last non-empty one, which may be shorter, and trailing ranks may own
+ * none (T = 5 over 4 ranks gives 2, 2, 1 and 0 rows). A shard padded to s
+ * rows is what an all-gather of equal-sized pieces moves.
+ *
+ *   num_tokens  T >= 0.
+ *   world       number of ranks, >= 1.
+ *   rank        0 .. world - 1.
+ *   row0, rows  out (host pointers): first row and row count of the shard.
+ *
+ * Pure host integer code: no CUDA call, no GPU needed.
+ * Errors: TW_ERR_INVALID_ARG (T < 0, world <= 0, rank out of range, a NULL
+ * output pointer).
+ */
+TW_API int tw_shard_rows(int64_t num_tokens, int world, int rank, int64_t* row0, int64_t* rows);
+
 /* Text of a tw_status value (static storage; never NULL). */
 TW_API const char* tw_strerror(int status);
 

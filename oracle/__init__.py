@@ -37,6 +37,13 @@ Functions and what pins each one (tests/test_oracle_*.py, ``-m "not gpu"``):
                                   [W] "The overlap trap" and "Fix one", the
                                   single-wave and threshold rules of "Fix
                                   one", and hand-computed cases.
+  shards.shard_rows               Row-by-row owner rule of the token-boundary
+                                  shards ([W] "Fix two"). Pinned by the
+                                  partition's invariants (every row owned
+                                  once, contiguous and in rank order, sizes
+                                  ceil(T/world) but the tail) and by
+                                  hand-computed cases (1024 over 8 ranks;
+                                  5 over 4 ranks).
   unfused.*                       The two-kernel (reduce, then standalone
                                   RMSNorm) baseline's numerics; pinned by the
                                   same closed forms.
@@ -44,4 +51,4 @@ Functions and what pins each one (tests/test_oracle_*.py, ``-m "not gpu"``):
 No function here is "parity unpinned".
 """
 
-from . import bf16, fused, planner, unfused  # noqa: F401
+from . import bf16, fused, planner, shards, unfused  # noqa: F401

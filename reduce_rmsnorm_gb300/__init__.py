@@ -21,6 +21,10 @@ The functions carry the C names:
     tw_fused_debug_smid(partials, residual, gamma, eps, out, smid_out, stream=None, sm_budget=0)
     tw_reduce_partials(partials, sum_out, stream=None)                 # unfused baseline
     tw_add_rmsnorm(sum_in, residual, gamma, eps, out, stream=None)     # unfused baseline
+    tw_shard_rows(num_tokens, world, rank)                              # token-boundary shard
+
+The token-shard form of the step across tensor-parallel ranks (all-to-all,
+fused step on the rank's shard, all-gather) is ``shard.TokenShardStep``.
 
 For launch-bound loops, ``FusedCall``, ``SplitCall``, ``WaveSplitCall`` and
 ``PlannedSplitCall`` marshal the arguments once and then make a single ctypes
@@ -48,7 +52,7 @@ DEFAULT_MIN_SPLIT_TOKENS = 1024
 EXPORTED = ("tw_fused_reduce_residual_rmsnorm", "tw_wave_split", "tw_run_split", "tw_strerror",
             "tw_launch_shape", "tw_device_status", "tw_fused_debug_smid", "tw_reduce_partials",
             "tw_add_rmsnorm", "tw_run_split_after", "tw_split_lookup", "tw_debug_wait_timeout",
-            "tw_run_wave_split")
+            "tw_run_wave_split", "tw_shard_rows")
 
 
 class TwError(RuntimeError):
@@ -114,6 +118,8 @@ def lib():
     L.tw_reduce_partials.restype = _int
     L.tw_add_rmsnorm.argtypes = [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp]
     L.tw_add_rmsnorm.restype = _int
+    L.tw_shard_rows.argtypes = [_i64, _int, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]
+    L.tw_shard_rows.restype = _int
     _lib = L
     return L
 
@@ -354,6 +360,16 @@ def tw_run_wave_split(ctas_unsplit, num_sms, partials, residual, gamma, eps, out
     del keep
     _check(st, "tw_run_wave_split")
     return p.value, s.value
+
+
+def tw_shard_rows(num_tokens, world, rank):
+    """(row0, rows) of `rank`'s token-boundary shard of a num_tokens batch
+    over `world` ranks: contiguous shards of ceil(T / world) rows in rank
+    order, the tail shorter."""
+    a, b = _i64(), _i64()
+    _check(lib().tw_shard_rows(int(num_tokens), int(world), int(rank), ctypes.byref(a),
+                               ctypes.byref(b)), "tw_shard_rows")
+    return a.value, b.value
 
 
 def _event(e):

@@ -119,3 +119,20 @@ extern "C" int tw_split_lookup(const int64_t* table_tokens, const int64_t* table
   }
   return tw_wave_split(num_tokens, ctas_unsplit, num_sms, opts, prefix_tokens, suffix_tokens);
 }
+
+// Token-boundary shard of one rank ([W] "Fix two": the reduce-scatter splits
+// the batch at token boundaries, so each rank normalises whole token rows).
+// Every rank's shard holds ceil(T / world) rows except at the tail: rank r
+// owns [min(r * s, T), min((r + 1) * s, T)) with s = ceil(T / world), so the
+// shards are contiguous, disjoint, in rank order, and cover every row once.
+extern "C" int tw_shard_rows(int64_t num_tokens, int world, int rank, int64_t* row0,
+                             int64_t* rows) {
+  if (!row0 || !rows) return TW_ERR_INVALID_ARG;
+  if (num_tokens < 0 || world <= 0 || rank < 0 || rank >= world) return TW_ERR_INVALID_ARG;
+  const int64_t s = ceil_div(num_tokens, world);
+  const int64_t a = std::min<int64_t>(static_cast<int64_t>(rank) * s, num_tokens);
+  const int64_t b = std::min<int64_t>(a + s, num_tokens);
+  *row0 = a;
+  *rows = b - a;
+  return TW_OK;
+}

@@ -167,3 +167,25 @@ def test_planner_threshold_mutant_is_caught(monkeypatch):
 
     monkeypatch.setattr(planner, "wave_split", no_threshold)
     assert _fails(pins.test_planner_golden)
+
+
+SHARD_PINS = (pins.test_shard_oracle_hand_cases, pins.test_shard_oracle_partition_invariants)
+
+
+def _owner_floor(t, T, world):
+    return t // max(T // world, 1)          # floor for ceil
+
+
+def _owner_interleaved(t, T, world):
+    return t % world                         # round-robin rows, not token ranges
+
+
+def _owner_reversed(t, T, world):
+    return world - 1 - t // -(-T // world)   # shards in reverse rank order
+
+
+@pytest.mark.parametrize("mutant", [_owner_floor, _owner_interleaved, _owner_reversed])
+def test_shard_mutants_are_caught(monkeypatch, mutant):
+    from oracle import shards
+    monkeypatch.setattr(shards, "owner", mutant)
+    assert _fails(*SHARD_PINS)

@@ -378,3 +378,38 @@ def test_fp64_oracle_against_50_digit_decimal_reference():
                 assert abs(float(y) - y64[a, b]) <= 1e-12 * abs(float(y)), (a, b)
             else:
                 assert y64[a, b] == 0
+
+
+# ------------------------------------------------------------------ token-boundary shards
+
+def test_shard_oracle_hand_cases():
+    """Hand-computed shards: the Llama-3.3-70B configuration's 8 x 128-token
+    shards, an uneven batch whose last rank owns nothing, and a single rank."""
+    from oracle import shards
+    assert [shards.shard_rows(1024, 8, r) for r in range(8)] == [(128 * r, 128) for r in range(8)]
+    assert [shards.shard_rows(5, 4, r) for r in range(4)] == [(0, 2), (2, 2), (4, 1), (5, 0)]
+    assert [shards.shard_rows(10, 3, r) for r in range(3)] == [(0, 4), (4, 4), (8, 2)]
+    assert shards.shard_rows(7, 1, 0) == (0, 7)
+    assert shards.shard_rows(0, 4, 2) == (0, 0)
+
+
+def test_shard_oracle_partition_invariants():
+    """For every T <= 70 and world <= 9: the shards are contiguous, in rank
+    order, cover every row exactly once, and hold ceil(T / world) rows each
+    except the tail. A mistake in the owner rule (floor for ceil, an offset
+    by one rank, interleaved rows) breaks one of these."""
+    from oracle import shards
+    for T in range(0, 71):
+        for world in range(1, 10):
+            s = -(-T // world)
+            got = [shards.shard_rows(T, world, r) for r in range(world)]
+            covered = []
+            nxt = 0
+            for r, (row0, rows) in enumerate(got):
+                assert rows >= 0 and row0 == min(nxt, T)
+                covered.extend(range(row0, row0 + rows))
+                nxt = row0 + rows
+                assert rows <= s
+                if nxt < T:
+                    assert rows == s
+            assert covered == list(range(T))
