@@ -174,6 +174,7 @@ class ClockSampler:
         import threading
         self.source = source
         self.samples = []
+        self.edges = {}
         self.lock = threading.Lock()
         self.t0 = self.t1 = None
         self.halt = threading.Event()
@@ -219,6 +220,14 @@ class ClockSampler:
     def take_now(self):
         self._take()
 
+    def take_edge(self, name):
+        """One sample reported on its own (not in the region's summary): taken
+        right before the region, while the warm-up steps still run, or right
+        after it."""
+        r = self.source.sample()
+        if r is not None:
+            self.edges[name] = {"sm_mhz": r["sm"], "reasons": r["reasons"]}
+
     def begin(self):
         self.t0 = time.perf_counter()
 
@@ -236,6 +245,8 @@ class ClockSampler:
         if out is not None:
             out["source"] = self.source.name
             out["window"] = "timed region (%.1f ms)" % ((self.t1 - self.t0) * 1e3)
+            if self.edges:
+                out["edges"] = self.edges
         return out
 
 
@@ -334,6 +345,131 @@ def make_sets(name, T_override, l2_bytes, device, N_override=0):
     return T, H, N, sets, per_set
 
 
+NOMINAL_HBM_GBS = 8000.0  # GB300's nominal HBM3e bandwidth, about 8 TB/s
+PRIME_CYCLES = 400_000     # ~0.2 ms at 2 GHz: the queue-priming delay before a timed region
+
+
+def _median(xs):
+    xs = sorted(xs)
+    return xs[len(xs) // 2]
+
+
+def after_gemm(tw, sets, eps, stream, H, N, reps=30):
+    """The fused step timed right after its real predecessor in a layer: the
+    row-parallel down projection of one rank, [T, 4H/N] x [4H/N, H] in bf16
+    (torch.matmul, cuBLAS), writing partial 0 of the set the step then reads.
+    Per rep, events around GEMM + fused step and, in a separate pass, around
+    the GEMM alone; the step's time is the difference of the medians."""
+    import torch
+    T = sets[0]["R"].shape[0]
+    K = 4 * H // N
+    dev = sets[0]["R"].device
+    gen = torch.Generator(device=dev).manual_seed(7)
+    x = torch.randn((T, K), generator=gen, device=dev).to(torch.bfloat16)
+    w = (torch.randn((K, H), generator=gen, device=dev) * K ** -0.5).to(torch.bfloat16)
+    fcalls = [tw.FusedCall(s["plist"], s["R"], s["G"], eps, s["out"], stream=stream) for s in sets]
+
+    def gemm(k):
+        torch.matmul(x, w, out=sets[k % len(sets)]["P"][0])
+
+    def timed(fused):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for k in range(3):
+                gemm(k)
+                if fused:
+                    fcalls[k % len(fcalls)]()
+            for k in range(reps):
+                evs[k][0].record(stream)
+                gemm(k)
+                if fused:
+                    fcalls[k % len(fcalls)]()
+                evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        return _median(a.elapsed_time(b) * 1e3 for a, b in evs)
+
+    pair_us = timed(True)
+    gemm_us = timed(False)
+    return {"pair_us": round(pair_us, 3), "gemm_us": round(gemm_us, 3),
+            "fused_us": round(pair_us - gemm_us, 3),
+            "gemm": "[%d,%d]x[%d,%d] bf16 torch.matmul" % (T, K, K, H), "reps": reps}
+
+
+def compact_sweep(tw, dev, l2, peak, reps=20):
+    """The rest of the metric in the default line: GB/s and tokens/s at
+    T = 1024 / 4096 / 16384 on the whole GPU, and GB/s per SM at SM budgets
+    2 / 4 / 8 / 16 for T = 8192 (H = 8192, N = 8). Inputs are made on the
+    device from a seeded generator with the workload's distributions (this
+    measures time only; parity runs on the synthetic CPU inputs). Each cell
+    times `reps` prepared launches back to back between one event pair, and
+    the median of per-launch event pairs over the same launches; inputs
+    rotate over enough sets to exceed 4x the L2, or one set is already larger
+    than that."""
+    import torch
+    H, N, eps = 8192, 8, 1e-5
+    gen = torch.Generator(device=dev).manual_seed(0)
+
+    def make(T):
+        per_set = (N + 2) * T * H * 2
+        out = []
+        for _ in range(max(1, math.ceil(4 * l2 / per_set))):
+            P = torch.empty((N, T, H), dtype=torch.bfloat16, device=dev)
+            for r in range(N):
+                P[r] = torch.randn((T, H), generator=gen, device=dev) * 0.02
+            R = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16)
+            G = (torch.randn((H,), generator=gen, device=dev) * 0.1 + 1).to(torch.bfloat16)
+            out.append(dict(P=P, R=R, G=G, out=torch.empty_like(R)))
+        return out
+
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+
+    def cell(sets, T, budget):
+        calls = [tw.FusedCall(s["P"], s["R"], s["G"], eps, s["out"], stream=stream,
+                              sm_budget=budget) for s in sets]
+        with torch.cuda.stream(stream):
+            for k in range(3):
+                calls[k % len(calls)]()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k in range(reps):
+                calls[k % len(calls)]()
+            b.record(stream)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for k in range(reps):
+                evs[k][0].record(stream)
+                calls[k % len(calls)]()
+                evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        b2b = a.elapsed_time(b) * 1e3 / reps
+        per = _median(x.elapsed_time(y) * 1e3 for x, y in evs)
+        nbytes = tw.bytes_per_call(T, H, N)
+        used = tw.tw_launch_shape(T, H, N, budget)["grid"]
+        gbs = nbytes / b2b / 1e3
+        return {"T": T, "sm_budget": budget or "full", "sms_used": used,
+                "us_b2b": round(b2b, 2), "GB_s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                "GB_s_per_sm": round(gbs / used, 2), "tokens_per_s": round(T / b2b * 1e6, 1),
+                "us_per_launch": round(per, 2),
+                "GB_s_per_launch": round(nbytes / per / 1e3, 1)}
+
+    cells = []
+    for T, budgets in ((1024, (0,)), (4096, (0,)), (16384, (0,)), (8192, (2, 4, 8, 16, 0))):
+        sets = make(T)
+        torch.cuda.synchronize()
+        for budget in budgets:
+            # budgeted launches are long (ms): fewer reps keep the block short
+            cells.append(cell(sets, T, budget))
+        del sets
+    torch.cuda.current_stream(dev).wait_stream(stream)
+    torch.cuda.empty_cache()
+    return {"H": H, "N": N, "reps": reps, "cells": cells,
+            "timing": "us_b2b: launches back to back between one event pair (GB_s, frac, "
+                      "GB_s_per_sm, tokens_per_s); us_per_launch: median of an event pair "
+                      "around each launch (launch latency included)"}
+
+
 def gpu_arm(args, rank, world):
     import torch
     import reduce_rmsnorm_gb300 as tw
@@ -388,6 +524,8 @@ def gpu_arm(args, rank, world):
             step_eager(k)
         for k in range(args.warmup):
             step(k)
+    if clocks:
+        clocks.take_edge("before")  # the warm-up steps are still running
     torch.cuda.synchronize()
     prefix, suffix = tw.tw_wave_split(T, C, PLANNER_SMS)
     launches_per_step = (1 if prefix > 0 else 0) + (1 if suffix > 0 else 0)
@@ -400,6 +538,11 @@ def gpu_arm(args, rank, world):
     if clocks:
         clocks.begin()
     with torch.cuda.stream(sa):
+        # A device-side delay ahead of the first event primes the launch queue:
+        # while it runs the host enqueues the first steps, so the region times
+        # the device running K steps back to back, not the host's first enqueue
+        # of an idle GPU (a short region otherwise carries ~10-20 us of it).
+        torch.cuda._sleep(PRIME_CYCLES)
         t_start.record(sa)
         for k in range(args.steps):
             step(args.warmup + k)
@@ -409,6 +552,7 @@ def gpu_arm(args, rank, world):
     torch.cuda.synchronize()
     if clocks:
         clocks.end()
+        clocks.take_edge("after")
     barrier(world)
     clk = clocks.stop() if clocks else None
     elapsed_ms = t_start.elapsed_time(t_end)
@@ -418,7 +562,7 @@ def gpu_arm(args, rank, world):
 
     # per-step distribution (separate pass: events between steps would
     # serialise the programmatic launch of the next step)
-    n_dist = min(args.steps, 500)
+    n_dist = min(max(args.steps, 50), 500)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_dist)]
     with torch.cuda.stream(sa):
@@ -451,10 +595,15 @@ def gpu_arm(args, rank, world):
                    "GB_s_on_fused_bytes": round(bytes_step / (u_ms / 1e3) / 1e9, 2),
                    "GB_s_on_own_bytes": round(u_bytes / (u_ms / 1e3) / 1e9, 2),
                    "fused_speedup": round(u_ms / mean_step_ms, 4)}
+    peak, peak_src = peak_hbm()
+    gemm_pair = sweep_block = None
+    if rank == 0 and not args.no_extras:
+        gemm_pair = after_gemm(tw, sets, eps, sa, H, N)
+        sweep_block = compact_sweep(tw, dev, l2, peak)
     assert tw.tw_device_status(reset=True) == 0, "a kernel gave up on a bounded wait"
 
-    peak, peak_src = peak_hbm()
     achieved = bytes_step / (mean_step_ms / 1e3) / 1e9
+    per_launch_us = step_us[len(step_us) // 2]
     traffic = ncu_traffic(args.workload if not args.tokens else None)
 
     result = None
@@ -475,19 +624,30 @@ def gpu_arm(args, rank, world):
                        "launch": "cuda graph per (input set, plan); plan computed every step"
                                  if args.mode == "graph" else
                                  "eager prepared calls, programmatic dependent launch",
+                       "queue": "a device-side delay before the first event primes the launch "
+                                "queue (the region times device execution of the K steps)",
                        "planner": {"ctas_unsplit": C, "num_sms": PLANNER_SMS},
                        "parallelism": "replicas" if world > 1 else "single-gpu",
                        "l2": "rotating %d input sets, %.1f MB total (L2 %.1f MB): inputs larger "
                              "than 4x L2" % (len(sets), len(sets) * per_set / 1e6, l2 / 1e6)},
             "tokens_per_s": round(T * args.steps * world / (elapsed_ms_max / 1e3), 1),
             "hbm_frac": round(value_gbs / peak, 4),
+            "hbm_frac_nominal": round(value_gbs / NOMINAL_HBM_GBS, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": peak_src, "per": "launch (one fused call per step)"
                          if launches_per_step == 1 else "step (%d concurrent launches)"
                          % launches_per_step,
                          "algorithmic_bytes": bytes_step,
-                         "duration": "mean over the timed region's %d steps" % args.steps},
+                         "duration": "mean over the timed region's %d steps" % args.steps,
+                         "frac_per_launch": round(bytes_step / per_launch_us / 1e3 / peak, 4),
+                         "frac_per_launch_note": "median of an event pair around each step "
+                                                 "(step_us), launch latency included",
+                         "frac_after_gemm": None if gemm_pair is None else
+                         round(bytes_step / gemm_pair["fused_us"] / 1e3 / peak, 4),
+                         "after_gemm": gemm_pair,
+                         "nominal_peak": NOMINAL_HBM_GBS,
+                         "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
             "step_us": {"median": round(step_us[len(step_us) // 2], 3),
                         "p10": round(step_us[len(step_us) // 10], 3),
                         "p90": round(step_us[(9 * len(step_us)) // 10], 3),
@@ -495,6 +655,7 @@ def gpu_arm(args, rank, world):
             "unfused": unfused, "cpu_baseline": cpu, "cpu_baseline_procs": cpu_procs, "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
+            "sweep": sweep_block,
         }
     return result
 
@@ -1026,6 +1187,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the after-GEMM timing and the compact sweep block")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-tokens", default="512,1024,2048,4096,8192,16384")
     ap.add_argument("--sweep-budgets", default="2,4,8,16,0")

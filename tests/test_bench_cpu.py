@@ -72,6 +72,18 @@ def test_clock_sampler_keeps_only_the_timed_region():
     c = s.stop()
     assert c["samples"] == 2 and c["sm_mhz"] == 2062.5 and c["reasons"] == ["sw_power_cap"]
     assert c["source"] == "fake" and c["window"].startswith("timed region")
+    assert "edges" not in c
+    # edge samples right before and after the region are reported on their own
+    e = bench.ClockSampler(Fake(), period_ms=10 ** 6)
+    e.take_edge("before")                              # 900
+    e.begin()
+    e.take_now()                                       # region: 900
+    e.end()
+    e.take_edge("after")
+    c = e.stop()
+    assert c["samples"] == 1
+    assert set(c["edges"]) == {"before", "after"}
+    assert c["edges"]["before"] == {"sm_mhz": 900.0, "reasons": ["sw_power_cap"]}
     empty = bench.ClockSampler(Fake(), period_ms=10 ** 6)
     empty.begin()
     empty.end()
