@@ -55,7 +55,6 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 // A "slot" is one 16-byte vector per consumer thread: 256 vectors, 4 KiB of a
 // source row. A chunk (the unit of one bulk copy per source) is VPT slots.
 constexpr int kSlotVec = kConsumerThreads;
@@ -163,10 +162,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ void consumer_barrier() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrierId), "n"(kConsumerThreads) : "memory");
-}
-
 // Asks L2 to fetch [src, src + bytes) (16-byte aligned, bytes a multiple of
 // 16). A hint only: nothing is returned to the thread and no memory is written.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
@@ -249,6 +244,24 @@ __device__ __forceinline__ void add8(const uint4 q, float a[8]) {
   add2(a[6], a[7], q.w);
 }
 
+// y[i] = (z[i] * rs) * gamma[i] for the 8 bf16 gamma values of q, as packed
+// fp32x2 multiplies (mul.rn.f32x2: two IEEE round-to-nearest products per
+// instruction, the same results as scalar multiplies in the same order).
+__device__ __forceinline__ void scale8(const float z[8], float rs, const uint4 q, float y[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint64_t r2;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r2) : "f"(rs));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint64_t a, g;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(z[2 * k]), "f"(z[2 * k + 1]));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(g) : "r"(w[k] << 16), "r"(w[k] & 0xffff0000u));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(r2));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(a) : "l"(g));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(y[2 * k]), "=f"(y[2 * k + 1]) : "l"(a));
+  }
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -309,17 +322,25 @@ __device__ __forceinline__ void reduce_vector(uint32_t src, uint32_t cbytes, int
 // Thread t of the consumers owns vectors t, t + 256, t + 512, ... of every row
 // (slot j = vector j * 256 + t) whatever VPT is, so the per-row arithmetic,
 // including the order of the sum of squares, depends only on H.
-template <int KMAX, int VPT, int NT, bool EXACT>
-__global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constant__ Params p) {
+// G:     independent pipelines sharing the CTA (1 or 2). Pipeline g owns a
+//        contiguous part of the CTA's rows, G-th of the ring, producer lanes
+//        16 g .. 16 g + N and consumer warps 8 g .. 8 g + 7; a second pipeline
+//        overlaps one row's epilogue with another row's reduction where the
+//        consumer work per byte caps an SM (small N under an SM budget).
+template <int KMAX, int VPT, int NT, bool EXACT, int G = 1>
+__global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
+    fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ float warp_ss[2][kConsumerWarps];
+  __shared__ float warp_ss[G][2][kConsumerWarps];
   __shared__ int abort_flag;
 
   constexpr int kChunkVec = kSlotVec * VPT;
   constexpr uint32_t kChunkBytes = kSlotBytes * VPT;
+  constexpr int kProducerWarp = G * kConsumerWarps;
   static_assert(KMAX % VPT == 0, "slots must fill whole chunks");
+  static_assert(G == 1 || NT <= 15, "two pipelines take at most 16 producer lanes each");
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -329,11 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   const int n = NT > 0 ? NT : p.n_partials;
   const int vpr = EXACT ? KMAX * kSlotVec : p.vec_per_row;
   const int chunks = EXACT ? KMAX / VPT : p.chunks;
-  const int stages = p.stages;
+  const int stages = p.stages;  // of each pipeline
   const uint32_t stage_bytes = static_cast<uint32_t>(n + 1) * kChunkBytes;
+  // rows of pipeline g: [part(g), part(g + 1))
+  auto part = [&](int g) { return row0 + (row1 - row0) * g / G; };
 
   if (tid == 0) {
-    for (int s = 0; s < stages; ++s) {
+    for (int s = 0; s < G * stages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kConsumerWarps);
     }
@@ -341,6 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     fence_mbar_init();
   }
   __syncthreads();
+  // Producer lane -> (pipeline, source): lane r for G = 1; lane 16 g + r for
+  // G = 2.
+  const int pg = G == 1 ? 0 : lane >> 4;
+  const int src_lane = G == 1 ? lane : (lane & 15);
   // Programmatic dependent launch: this CTA may be resident before the
   // previous kernel in the stream has finished. Nothing above read or wrote
   // global memory. A CTA that lands on an SM the previous kernel has already
@@ -350,32 +377,42 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   // is the device's point of coherence and so holds the previous kernel's
   // writes. Then wait until that kernel has completed and its writes are
   // visible, and allow the next kernel in the stream to start launching.
-  if (p.prefetch_bytes != 0 && warp == kConsumerWarps && lane <= n && row1 > row0) {
-    const char* src = reinterpret_cast<const char*>((lane < n ? p.partials[lane] : p.residual) +
-                                                    row0 * vpr);
-    const long long avail = (row1 - row0) * vpr * 16;
-    const uint32_t total = static_cast<uint32_t>(
-        static_cast<long long>(p.prefetch_bytes) < avail ? p.prefetch_bytes : avail);
-    for (uint32_t off = 0; off < total; off += kPrefetchPiece)
-      prefetch_l2(src + off, total - off < kPrefetchPiece ? total - off : kPrefetchPiece);
+  if (p.prefetch_bytes != 0 && warp == kProducerWarp && src_lane <= n && pg < G) {
+    const long long ra = part(pg), rb = part(pg + 1);
+    if (rb > ra) {
+      const char* src = reinterpret_cast<const char*>(
+          (src_lane < n ? p.partials[src_lane] : p.residual) + ra * vpr);
+      const long long avail = (rb - ra) * vpr * 16;
+      const uint32_t want = (p.prefetch_bytes / G) & ~15u;
+      const uint32_t total =
+          static_cast<uint32_t>(static_cast<long long>(want) < avail ? want : avail);
+      for (uint32_t off = 0; off < total; off += kPrefetchPiece)
+        prefetch_l2(src + off, total - off < kPrefetchPiece ? total - off : kPrefetchPiece);
+    }
   }
   grid_dependency_wait();
   grid_launch_dependents();
   if (tid == 0 && p.smid_out) p.smid_out[blockIdx.x] = static_cast<int>(sm_id());
   volatile int* abort = &abort_flag;
 
-  if (warp == kConsumerWarps) {
-    // ---------------- producer: lanes 0..N stream (row, chunk) items into the
-    // ring; lane r < N copies partial r, lane N the residual.
-    if (lane > n) return;
-    const unsigned lanes = n + 1 == 32 ? 0xffffffffu : ((1u << (n + 1)) - 1u);
+  if (warp == kProducerWarp) {
+    // ---------------- producer: lanes 0..N of pipeline g stream its (row,
+    // chunk) items into its part of the ring; lane r < N copies partial r,
+    // lane N the residual.
+    if (src_lane > n || pg >= G) return;
+    const unsigned lanes = (n + 1 == 32 ? 0xffffffffu : ((1u << (n + 1)) - 1u)) << (16 * pg);
+    const int lead = 16 * pg;  // the pipeline's first lane
+    uint64_t* full = full_bar + pg * stages;
+    uint64_t* empty = empty_bar + pg * stages;
+    unsigned char* my_ring = ring + static_cast<size_t>(pg) * stages * stage_bytes;
     // Evict-first or normal L2 policy for the loads, chosen per call on the
     // host (launch_fused).
     const uint64_t policy = p.l2_stream ? l2_evict_first_policy() : l2_evict_normal_policy();
-    const uint4* src_base = lane < n ? p.partials[lane] : p.residual;
-    const long long items = (row1 - row0) * chunks;
+    const uint4* src_base = src_lane < n ? p.partials[src_lane] : p.residual;
+    const long long ra = part(pg), rb = part(pg + 1);
+    const long long items = (rb - ra) * chunks;
     long long issued = 0;
-    long long row = row0;
+    long long row = ra;
     int chunk = 0, s = 0;
     uint32_t round_parity = 0;  // parity of the current pass over the ring
     bool first_pass = true;
@@ -384,18 +421,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
       const int v0 = chunk * kChunkVec;
       const int nvec = EXACT ? kChunkVec : min(kChunkVec, vpr - v0);
       const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
-      if (lane == 0) {
-        if (!first_pass) ok = wait_phase(&empty_bar[s], round_parity ^ 1u, abort, 2u);
-        if (ok) mbar_arrive_expect_tx(&full_bar[s], bytes * static_cast<uint32_t>(n + 1));
+      if (src_lane == 0) {
+        if (!first_pass) ok = wait_phase(&empty[s], round_parity ^ 1u, abort, 2u);
+        if (ok) mbar_arrive_expect_tx(&full[s], bytes * static_cast<uint32_t>(n + 1));
       }
-      if (!__shfl_sync(lanes, ok, 0)) break;
-      bulk_load(ring + static_cast<size_t>(s) * stage_bytes + lane * kChunkBytes,
-                src_base + row * vpr + v0, bytes, &full_bar[s], policy);
+      if (!__shfl_sync(lanes, ok, lead)) break;
+      bulk_load(my_ring + static_cast<size_t>(s) * stage_bytes + src_lane * kChunkBytes,
+                src_base + row * vpr + v0, bytes, &full[s], policy);
       ++issued;
       if (++chunk == chunks) { chunk = 0; ++row; }
       if (++s == stages) { s = 0; round_parity ^= 1u; first_pass = false; }
     }
-    if (lane == 0) {
+    if (src_lane == 0) {
       // The producer owns the drain: every copy this CTA issued lands before
       // the CTA can exit, whether or not a consumer gave up a wait (possibly
       // after the producer left its loop). The last item issued on each stage
@@ -405,15 +442,21 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
       const long long last = issued - 1;
       for (int st = 0; st < stages && st <= last; ++st) {
         const long long it_last = last - ((last - st) % stages);
-        drain_phase(&full_bar[st], static_cast<uint32_t>((it_last / stages) & 1));
+        drain_phase(&full[st], static_cast<uint32_t>((it_last / stages) & 1));
       }
     }
     return;
   }
 
-  // ---------------- consumers: 8 warps; thread t owns slots j (vector j*256 + t)
-  const int t = tid;
-  const uint32_t ring_base = smem_addr(ring) + static_cast<uint32_t>(t) * 16u;
+  // ---------------- consumers: 8 warps per pipeline; thread t owns slots j
+  // (vector j*256 + t)
+  const int g = warp / kConsumerWarps;
+  const int wg = warp % kConsumerWarps;
+  const int t = tid - g * kConsumerThreads;
+  uint64_t* full = full_bar + g * stages;
+  uint64_t* empty = empty_bar + g * stages;
+  const uint32_t ring_base = smem_addr(ring) + static_cast<uint32_t>(g * stages) * stage_bytes +
+                             static_cast<uint32_t>(t) * 16u;
   // gamma stays in registers for the CTA's whole row range (read once per CTA)
   constexpr bool kGammaRegs = KMAX <= 8;
   uint4 g_reg[kGammaRegs ? KMAX : 1];
@@ -427,13 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
   int s = 0;
   uint32_t parity = 0;
   float z[KMAX][8];
-  for (long long row = row0; row < row1; ++row) {
+  const long long ra = part(g), rb = part(g + 1);
+  for (long long row = ra; row < rb; ++row) {
     float ss = 0.0f;
     uint4* res_row = p.residual + row * vpr;
 #pragma unroll
     for (int c = 0; c < KMAX / VPT; ++c) {
       if (c < chunks) {
-        wait_phase(&full_bar[s], parity, abort, 1u);
+        wait_phase(&full[s], parity, abort, 1u);
         const uint32_t stage = ring_base + static_cast<uint32_t>(s) * stage_bytes;
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
@@ -442,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
             reduce_vector<NT>(stage + u * kSlotBytes, kChunkBytes, n, z[j]);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
         for (int u = 0; u < VPT; ++u) {
           const int j = c * VPT + u;
@@ -458,28 +502,219 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const __grid_constan
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const int buf = static_cast<int>((row - row0) & 1);
-    if (lane == 0) warp_ss[buf][warp] = ss;
-    consumer_barrier();
+    const int buf = static_cast<int>((row - ra) & 1);
+    if (lane == 0) warp_ss[g][buf][wg] = ss;
+    asm volatile("bar.sync %0, %1;" ::"r"(kConsumerBarrierId + g), "n"(kConsumerThreads)
+                 : "memory");
     float total = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) total += warp_ss[buf][w];
+    for (int w = 0; w < kConsumerWarps; ++w) total += warp_ss[g][buf][w];
     const float rs = rsqrtf(total / p.hidden + p.eps);
     uint4* out_row = p.out + row * vpr;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       const int v = j * kSlotVec + t;
       if (EXACT || v < vpr) {
-        float g[8], y[8];
-        if constexpr (kGammaRegs) load8(g_reg[j], g);
-        else load8(__ldg(p.gamma + v), g);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y[i] = (z[j][i] * rs) * g[i];
+        float y[8];
+        if constexpr (kGammaRegs) scale8(z[j], rs, g_reg[j], y);
+        else scale8(z[j], rs, __ldg(p.gamma + v), y);
         // With evict-first loads the output is stored streaming too, so its
         // lines drain during this launch; with normal loads the store policy
         // measured within 0.2%. A kernel that reads Y right after still finds
         // it unless L2 needs the room. The residual keeps the default policy
         // (evict-first there measured -1%).
+        if (p.l2_stream) __stcs(out_row + v, pack8(y));
+        else out_row[v] = pack8(y);
+      }
+    }
+  }
+}
+
+// Row-ring form: one bulk copy per (row, source), so a stage holds one
+// source's whole row (KMAX 4 KiB slots: 16-64 KiB), and G independent
+// pipelines share the CTA. Pipeline g owns a contiguous part of the CTA's rows,
+// producer lane g, its own part of the ring (p.stages stages) and consumer
+// warps 8g .. 8g + 7; each pipeline is consumed in order by its own warps, as
+// in fused_kernel. Against fused_kernel it issues (N + 1) copies per row
+// instead of (N + 1) * chunks, of 16 KiB and more (the TMA issue cost is
+// nearly flat in size up to 8 KiB, so small copies cap an SM under an SM
+// budget), and with G = 2 two rows are reduced at once (the consumer work per
+// byte is what caps an SM at small N). Thread t of a pipeline owns the same
+// vectors t + 256 j as in fused_kernel and adds the sources in the same rank
+// order, then the residual, so rows are bitwise those of fused_kernel.
+template <int KMAX, int G, int NT, bool EXACT>
+__global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
+    rowring_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
+  __shared__ float warp_ss[G][2][kConsumerWarps];
+  __shared__ int abort_flag;
+
+  constexpr uint32_t kStageBytes = KMAX * kSlotBytes;
+  constexpr int kProducerWarp = G * kConsumerWarps;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const long long grid = gridDim.x;
+  const long long row0 = static_cast<long long>(blockIdx.x) * p.rows / grid;
+  const long long row1 = static_cast<long long>(blockIdx.x + 1) * p.rows / grid;
+  const int n = NT > 0 ? NT : p.n_partials;
+  const int vpr = EXACT ? KMAX * kSlotVec : p.vec_per_row;
+  const int spp = p.stages;  // stages of each pipeline
+  // rows of pipeline g: [part(g), part(g + 1))
+  auto part = [&](int g) { return row0 + (row1 - row0) * g / G; };
+
+  if (tid == 0) {
+    for (int s = 0; s < G * spp; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // L2 warm-up before the dependency wait, as in fused_kernel: lane r asks for
+  // the first bytes of source r's rows of each pipeline.
+  if (p.prefetch_bytes != 0 && warp == kProducerWarp && lane <= n) {
+    const uint4* base = lane < n ? p.partials[lane] : p.residual;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const long long ra = part(g), rb = part(g + 1);
+      if (rb <= ra) continue;
+      const char* src = reinterpret_cast<const char*>(base + ra * vpr);
+      const long long avail = (rb - ra) * vpr * 16;
+      const uint32_t want = (p.prefetch_bytes / G) & ~15u;
+      const uint32_t total =
+          static_cast<uint32_t>(static_cast<long long>(want) < avail ? want : avail);
+      for (uint32_t off = 0; off < total; off += kPrefetchPiece)
+        prefetch_l2(src + off, total - off < kPrefetchPiece ? total - off : kPrefetchPiece);
+    }
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (tid == 0 && p.smid_out) p.smid_out[blockIdx.x] = static_cast<int>(sm_id());
+  volatile int* abort = &abort_flag;
+
+  if (warp == kProducerWarp) {
+    // ---------------- producer lane g feeds pipeline g: items (row, source),
+    // sources 0..N-1 then the residual, one whole-row bulk copy each.
+    if (lane >= G) return;
+    const int g = lane;
+    uint64_t* full = full_bar + g * spp;
+    uint64_t* empty = empty_bar + g * spp;
+    unsigned char* my_ring = ring + static_cast<size_t>(g) * spp * kStageBytes;
+    const uint64_t policy = p.l2_stream ? l2_evict_first_policy() : l2_evict_normal_policy();
+    const uint32_t bytes = static_cast<uint32_t>(vpr) * 16u;
+    const long long ra = part(g), rb = part(g + 1);
+    const long long items = (rb - ra) * (n + 1);
+    long long issued = 0;
+    long long row = ra;
+    int r = 0, s = 0;
+    uint32_t round_parity = 0;
+    bool first_pass = true;
+    for (long long it = 0; it < items; ++it) {
+      if (!first_pass && !wait_phase(&empty[s], round_parity ^ 1u, abort, 2u)) break;
+      mbar_arrive_expect_tx(&full[s], bytes);
+      const uint4* src = r < n ? p.partials[r] : p.residual;
+      bulk_load(my_ring + static_cast<size_t>(s) * kStageBytes, src + row * vpr, bytes, &full[s],
+                policy);
+      ++issued;
+      if (++r > n) { r = 0; ++row; }
+      if (++s == spp) { s = 0; round_parity ^= 1u; first_pass = false; }
+    }
+    // The producer owns the drain (see fused_kernel): every copy it issued
+    // lands before the CTA can exit.
+    const long long last = issued - 1;
+    for (int st = 0; st < spp && st <= last; ++st) {
+      const long long it_last = last - ((last - st) % spp);
+      drain_phase(&full[st], static_cast<uint32_t>((it_last / spp) & 1));
+    }
+    return;
+  }
+
+  // ---------------- consumers: pipeline g = warp / 8; thread t owns slots j
+  // (vector j * 256 + t) of every row of the pipeline
+  const int g = warp / kConsumerWarps;
+  const int wg = warp % kConsumerWarps;
+  const int t = tid - g * kConsumerThreads;
+  uint64_t* full = full_bar + g * spp;
+  uint64_t* empty = empty_bar + g * spp;
+  const uint32_t ring_base = smem_addr(ring) + static_cast<uint32_t>(g * spp) * kStageBytes +
+                             static_cast<uint32_t>(t) * 16u;
+  constexpr bool kGammaRegs = KMAX <= 8;
+  uint4 g_reg[kGammaRegs ? KMAX : 1];
+  if constexpr (kGammaRegs) {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const int v = j * kSlotVec + t;
+      g_reg[j] = (EXACT || v < vpr) ? __ldg(p.gamma + v) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  int s = 0;
+  uint32_t parity = 0;
+  float z[KMAX][8];
+  const long long ra = part(g), rb = part(g + 1);
+  for (long long row = ra; row < rb; ++row) {
+    // source r's whole row is one stage: z = P_0, then += P_1 .. P_{N-1}, += R
+    auto take = [&](bool first) {
+      wait_phase(&full[s], parity, abort, 1u);
+      const uint32_t stage = ring_base + static_cast<uint32_t>(s) * kStageBytes;
+      // loads of up to 8 slots issue together, then their adds
+      constexpr int kBatch = KMAX < 8 ? KMAX : 8;
+#pragma unroll
+      for (int j0 = 0; j0 < KMAX; j0 += kBatch) {
+        uint4 q[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (EXACT || (j0 + u) * kSlotVec + t < vpr) q[u] = lds128(stage + (j0 + u) * kSlotBytes);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (EXACT || (j0 + u) * kSlotVec + t < vpr) {
+            if (first) load8(q[u], z[j0 + u]);
+            else add8(q[u], z[j0 + u]);
+          }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == spp) { s = 0; parity ^= 1u; }
+    };
+    take(true);
+    if constexpr (NT > 0) {
+#pragma unroll
+      for (int r = 1; r <= NT; ++r) take(false);
+    } else {
+      for (int r = 1; r <= n; ++r) take(false);
+    }
+    float ss = 0.0f;
+    uint4* res_row = p.residual + row * vpr;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const int v = j * kSlotVec + t;
+      if (EXACT || v < vpr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(z[j][i], z[j][i], ss);
+        res_row[v] = pack8(z[j]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const int buf = static_cast<int>((row - ra) & 1);
+    if (lane == 0) warp_ss[g][buf][wg] = ss;
+    asm volatile("bar.sync %0, %1;" ::"r"(kConsumerBarrierId + g), "n"(kConsumerThreads)
+                 : "memory");
+    float total = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) total += warp_ss[g][buf][w];
+    const float rs = rsqrtf(total / p.hidden + p.eps);
+    uint4* out_row = p.out + row * vpr;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const int v = j * kSlotVec + t;
+      if (EXACT || v < vpr) {
+        float y[8];
+        if constexpr (kGammaRegs) scale8(z[j], rs, g_reg[j], y);
+        else scale8(z[j], rs, __ldg(p.gamma + v), y);
         if (p.l2_stream) __stcs(out_row + v, pack8(y));
         else out_row[v] = pack8(y);
       }
@@ -531,7 +766,27 @@ const KernelFn kVpt1[2][5][2] = {
     {TW_V1(1, false), TW_V1(2, false), TW_V1(4, false), TW_V1(8, false), TW_V1(16, false)},
     {TW_V1(1, true), TW_V1(2, true), TW_V1(4, true), TW_V1(8, true), TW_V1(16, true)}};
 #undef TW_V1
-constexpr int kNumKernels = 72 + 20;
+// Two-pipeline instances, all at KMAX = 4 (H/8 in 513..1024). The chunk ring
+// with 8 KiB chunks for N = 1..4 (N = 4 only for whole-chunk rows: the ragged
+// form spills at the two-pipeline register cap of 96), and the row ring for
+// whole-chunk rows (H = 8192) with N = 9..15 (runtime N) and 16.
+const KernelFn kChunkTwo[2][4] = {
+    {fused_kernel<4, 2, 1, false, 2>, fused_kernel<4, 2, 2, false, 2>,
+     fused_kernel<4, 2, 3, false, 2>, nullptr},
+    {fused_kernel<4, 2, 1, true, 2>, fused_kernel<4, 2, 2, true, 2>,
+     fused_kernel<4, 2, 3, true, 2>, fused_kernel<4, 2, 4, true, 2>}};
+const KernelFn kRowTwo[2] = {rowring_kernel<4, 2, 0, true>, rowring_kernel<4, 2, 16, true>};
+constexpr int kNumKernels = 92 + 8 + 2;
+
+// The kernel instance for a launch, and what its launch needs.
+struct Choice {
+  KernelFn fn;
+  int index;    // attribute-cache slot
+  int kmax;
+  int rowring;  // 0: chunk ring (fused_kernel); 1: row ring (rowring_kernel)
+  int groups;   // pipelines per CTA
+  int vpt;      // chunk ring: slots per chunk
+};
 
 // Per-device attributes, queried once; the launch path reads them without a
 // lock once `ready` is set (the flags live in static storage, so they start
@@ -571,22 +826,54 @@ int partials_index_vpt1(int n) { return n == 16 ? 1 : 0; }
 
 int vpt_for(int n) { return n <= 8 ? 2 : 1; }
 
-// Which instance serves (H/8 vectors, N): its table index and kernel.
-void select_kernel(int vpr, int n, int* index, KernelFn* fn, int* kmax) {
+// Which instance serves a launch of `rows` rows of H/8 = vpr vectors over
+// `grid` CTAs on a GPU of `sms` SMs. Every form gives bitwise the same rows
+// (same thread-to-vector map, same order of every sum), so the choice is by
+// speed alone. Measured back to back, interleaved, at H = 8192:
+//  * N <= 4, some CTA owning >= 4 rows: the chunk ring with two pipelines.
+//    Per SM at an 8-SM budget (T = 4096) N = 1 78 -> 102 GB/s, 2: 88 -> 116,
+//    3: 98 -> 121, 4: 107 -> 108; at full GPU 0-5% faster for T >= 1024, but
+//    6% slower with ~3 rows per CTA (T = 512, N = 4), hence the row floor.
+//  * N >= 9, whole-chunk rows, a grid of at most half the SMs: the row ring
+//    with two pipelines, whose 16 KiB copies lift the per-SM rate from 83-95
+//    to 112 GB/s at an 8-SM budget. At full GPU, where an SM needs ~45 GB/s,
+//    the chunk ring is 2-4% faster.
+//  * otherwise the chunk ring with one pipeline.
+Choice select_kernel(int vpr, int n, int64_t rows, int grid, int sms) {
+  Choice c;
   const int vpt = vpt_for(n);
   const int chunks = (vpr + kSlotVec * vpt - 1) / (kSlotVec * vpt);
   const int k = log2_pow2_at_least(chunks * vpt);  // KMAX = 2^k
-  *kmax = 1 << k;
+  c.kmax = 1 << k;
+  c.rowring = 0;
+  c.groups = 1;
+  c.vpt = vpt;
   const int exact = vpr == (1 << k) * kSlotVec ? 1 : 0;
+  const bool four_rows = rows >= 4 * static_cast<int64_t>(grid);
+  if (vpt == 2 && k == 2 && four_rows && (n <= 3 || (n == 4 && exact))) {
+    c.groups = 2;
+    c.index = 92 + exact * 4 + (n - 1);
+    c.fn = kChunkTwo[exact][n - 1];
+    return c;
+  }
+  if (n >= 9 && vpr == 4 * kSlotVec && 2 * grid <= sms) {
+    c.rowring = 1;
+    c.groups = 2;
+    c.kmax = 4;
+    c.index = 100 + (n == 16 ? 1 : 0);
+    c.fn = kRowTwo[n == 16 ? 1 : 0];
+    return c;
+  }
   if (vpt == 2) {
     const int ki = k - 1, ni = partials_index_vpt2(n);  // KMAX 2..16
-    *index = exact * 36 + ki * 9 + ni;
-    *fn = kVpt2[exact][ki][ni];
+    c.index = exact * 36 + ki * 9 + ni;
+    c.fn = kVpt2[exact][ki][ni];
   } else {
     const int ni = partials_index_vpt1(n);  // KMAX 1..16
-    *index = 72 + exact * 10 + k * 2 + ni;
-    *fn = kVpt1[exact][k][ni];
+    c.index = 72 + exact * 10 + k * 2 + ni;
+    c.fn = kVpt1[exact][k][ni];
   }
+  return c;
 }
 
 int device_info(DeviceInfo** out) {
@@ -610,18 +897,30 @@ int device_info(DeviceInfo** out) {
   return TW_OK;
 }
 
-int shape_for(const DeviceInfo& d, int64_t rows, int n, int sm_budget, LaunchShape* shape) {
-  const int stage_bytes = (n + 1) * kSlotBytes * vpt_for(n);
-  int stages = (d.smem_optin - kStaticSmemReserve) / stage_bytes;
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2) return TW_ERR_UNSUPPORTED;
+// One CTA per SM, at most sm_budget (0: all) and at most one per row.
+int grid_for(const DeviceInfo& d, int64_t rows, int sm_budget) {
   int grid = d.sms;
   if (sm_budget > 0 && sm_budget < grid) grid = sm_budget;
   if (rows < grid) grid = static_cast<int>(rows);
+  return grid;
+}
+
+// The launch of `rows` rows: the instance (*choice) and its shape.
+int shape_for(const DeviceInfo& d, int64_t rows, int64_t hidden, int n, int sm_budget,
+              Choice* choice, LaunchShape* shape) {
+  const int grid = grid_for(d, rows, sm_budget);
+  const Choice c = select_kernel(static_cast<int>(hidden / 8), n, rows, grid, d.sms);
+  // one stage: a source's row (row ring) or a chunk of every source (chunk ring)
+  const int stage_bytes = c.rowring ? c.kmax * kSlotBytes : (n + 1) * kSlotBytes * c.vpt;
+  int stages = (d.smem_optin - kStaticSmemReserve) / (c.groups * stage_bytes);
+  if (stages > kMaxStages / c.groups) stages = kMaxStages / c.groups;
+  if (stages < 2) return TW_ERR_UNSUPPORTED;
   shape->grid = grid;
-  shape->threads = kThreads;
-  shape->smem_bytes = stages * stage_bytes;
+  shape->threads = c.groups * kConsumerThreads + 32;
+  shape->smem_bytes = stages * stage_bytes * c.groups;
   shape->stages = stages;
+  shape->kmax = c.kmax;
+  *choice = c;
   return TW_OK;
 }
 
@@ -631,20 +930,17 @@ int plan_launch(int64_t rows, int64_t hidden, int n, int sm_budget, LaunchShape*
   DeviceInfo* d = nullptr;
   int st = device_info(&d);
   if (st != TW_OK) return st;
-  st = shape_for(*d, rows, n, sm_budget, shape);
-  if (st != TW_OK) return st;
-  int index = 0;
-  KernelFn fn = nullptr;
-  select_kernel(static_cast<int>(hidden / 8), n, &index, &fn, &shape->kmax);
-  return TW_OK;
+  Choice c;
+  return shape_for(*d, rows, hidden, n, sm_budget, &c, shape);
 }
 
 int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* smid_out) {
   DeviceInfo* d = nullptr;
   int st = device_info(&d);
   if (st != TW_OK) return st;
+  Choice choice;
   LaunchShape shape;
-  st = shape_for(*d, a.rows, a.n, sm_budget, &shape);
+  st = shape_for(*d, a.rows, a.hidden, a.n, sm_budget, &choice, &shape);
   if (st != TW_OK) return st;
   if (shape.grid <= 0) return TW_OK;
 
@@ -681,15 +977,14 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
   p.rows = a.rows;
   p.vec_per_row = static_cast<int>(a.hidden / 8);
   p.n_partials = a.n;
-  const int chunk_vec = kSlotVec * vpt_for(a.n);
+  const int chunk_vec = kSlotVec * (choice.rowring ? 1 : choice.vpt);  // row ring: unused
   p.chunks = (p.vec_per_row + chunk_vec - 1) / chunk_vec;
   p.stages = shape.stages;
   p.eps = a.eps;
   p.hidden = static_cast<float>(a.hidden);
 
-  int index = 0, kmax = 0;
-  KernelFn fn = nullptr;
-  select_kernel(p.vec_per_row, a.n, &index, &fn, &kmax);
+  const KernelFn fn = choice.fn;
+  const int index = choice.index;
   if (!d->attr_done[index].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!d->attr_done[index].load(std::memory_order_relaxed)) {
@@ -706,7 +1001,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
   // prefetch hint goes out before it).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(shape.grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(shape.threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(shape.smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -303,6 +303,28 @@ def test_sm_budget_bitwise(budget):
     assert_same(ref[1], got[1])
 
 
+@pytest.mark.parametrize("H,N", [(8192, 1), (8192, 2), (8192, 3), (8192, 4), (6152, 1),
+                                 (6152, 3), (8192, 9), (8192, 12), (8192, 16)])
+def test_kernel_forms_bitwise(H, N):
+    """The launch picks among kernel forms by speed: one or two pipelines per
+    CTA, chunk ring or row ring. Every form must give the same rows bit for
+    bit. T = 600 on the whole GPU (under 4 rows per CTA, a grid over half the
+    SMs) takes the one-pipeline chunk ring; an 8-SM budget takes the
+    two-pipeline form for these shapes. The launch shapes are checked to
+    differ, so the comparison is between two forms."""
+    T = 600
+    full = tw.tw_launch_shape(T, H, N, 0)
+    b8 = tw.tw_launch_shape(T, H, N, 8)
+    assert full["threads"] == 288 and b8["threads"] == 544, (full, b8)
+    p, r, g = synth.make_inputs(T, H, N, 0.02, seed=H + 3 * N)
+    ref = run(p, r, g, sm_budget=0)
+    got = run(p, r, g, sm_budget=8)
+    assert_same(ref[0], got[0])
+    assert_same(ref[1], got[1])
+    rows = [0, 1, 299, 300, 598, 599] + list(range(7, 600, 37))
+    check_rows(p, r, g, EPS, got[0], got[1], rows=rows)
+
+
 def test_shards_bitwise_llama70b():
     """8 token-boundary shards of 128 rows, each launched on its own, equal the
     whole T=1024 batch bit for bit ([W] "Fix two": the norm is per token, so a
