@@ -262,6 +262,13 @@ __device__ __forceinline__ void scale8(const float z[8], float rs, const uint4 q
   }
 }
 
+// Sum of the 8 warp partials in warp order, read as two 16-byte loads.
+__device__ __forceinline__ float warp_total(const float* w8) {
+  const float4 a = *reinterpret_cast<const float4*>(w8);
+  const float4 b = *reinterpret_cast<const float4*>(w8 + 4);
+  return ((((((a.x + a.y) + a.z) + a.w) + b.x) + b.y) + b.z) + b.w;
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -333,7 +340,7 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ float warp_ss[G][2][kConsumerWarps];
+  __shared__ __align__(16) float warp_ss[G][2][kConsumerWarps];
   __shared__ int abort_flag;
 
   constexpr int kChunkVec = kSlotVec * VPT;
@@ -355,14 +362,13 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   // rows of pipeline g: [part(g), part(g + 1))
   auto part = [&](int g) { return row0 + (row1 - row0) * g / G; };
 
-  if (tid == 0) {
-    for (int s = 0; s < G * stages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kConsumerWarps);
-    }
-    abort_flag = 0;
+  // thread s sets up stage s's two barriers
+  if (tid < G * stages) {
+    mbar_init(&full_bar[tid], 1);
+    mbar_init(&empty_bar[tid], kConsumerWarps);
     fence_mbar_init();
   }
+  if (tid == 0) abort_flag = 0;
   __syncthreads();
   // Producer lane -> (pipeline, source): lane r for G = 1; lane 16 g + r for
   // G = 2.
@@ -506,9 +512,7 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
     if (lane == 0) warp_ss[g][buf][wg] = ss;
     asm volatile("bar.sync %0, %1;" ::"r"(kConsumerBarrierId + g), "n"(kConsumerThreads)
                  : "memory");
-    float total = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) total += warp_ss[g][buf][w];
+    const float total = warp_total(warp_ss[g][buf]);
     const float rs = rsqrtf(total / p.hidden + p.eps);
     uint4* out_row = p.out + row * vpr;
 #pragma unroll
@@ -548,7 +552,7 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kMaxStages];
-  __shared__ float warp_ss[G][2][kConsumerWarps];
+  __shared__ __align__(16) float warp_ss[G][2][kConsumerWarps];
   __shared__ int abort_flag;
 
   constexpr uint32_t kStageBytes = KMAX * kSlotBytes;
@@ -565,14 +569,13 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   // rows of pipeline g: [part(g), part(g + 1))
   auto part = [&](int g) { return row0 + (row1 - row0) * g / G; };
 
-  if (tid == 0) {
-    for (int s = 0; s < G * spp; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kConsumerWarps);
-    }
-    abort_flag = 0;
+  // thread s sets up stage s's two barriers
+  if (tid < G * spp) {
+    mbar_init(&full_bar[tid], 1);
+    mbar_init(&empty_bar[tid], kConsumerWarps);
     fence_mbar_init();
   }
+  if (tid == 0) abort_flag = 0;
   __syncthreads();
   // L2 warm-up before the dependency wait, as in fused_kernel: lane r asks for
   // the first bytes of source r's rows of each pipeline.
@@ -703,9 +706,7 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
     if (lane == 0) warp_ss[g][buf][wg] = ss;
     asm volatile("bar.sync %0, %1;" ::"r"(kConsumerBarrierId + g), "n"(kConsumerThreads)
                  : "memory");
-    float total = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) total += warp_ss[g][buf][w];
+    const float total = warp_total(warp_ss[g][buf]);
     const float rs = rsqrtf(total / p.hidden + p.eps);
     uint4* out_row = p.out + row * vpr;
 #pragma unroll
@@ -756,11 +757,17 @@ using KernelFn = void (*)(Params);
 #define TW_V2L(K, E) {fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 1, E>, fused_kernel<K, 2, 2, E>, \
                       fused_kernel<K, 2, 4, E>, fused_kernel<K, 2, 8, E>, fused_kernel<K, 2, 0, E>, \
                       fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 0, E>, fused_kernel<K, 2, 0, E>}
+// KMAX 16: N = 4 takes the runtime-N instance (the compile-time one spilled
+// at the 168-register cap of a 9-warp CTA).
+#define TW_V2XL(E) {fused_kernel<16, 2, 0, E>, fused_kernel<16, 2, 1, E>, fused_kernel<16, 2, 2, E>, \
+                    fused_kernel<16, 2, 0, E>, fused_kernel<16, 2, 8, E>, fused_kernel<16, 2, 0, E>, \
+                    fused_kernel<16, 2, 0, E>, fused_kernel<16, 2, 0, E>, fused_kernel<16, 2, 0, E>}
 const KernelFn kVpt2[2][4][9] = {
-    {TW_V2S(2, false), TW_V2S(4, false), TW_V2L(8, false), TW_V2L(16, false)},
-    {TW_V2S(2, true), TW_V2S(4, true), TW_V2L(8, true), TW_V2L(16, true)}};
+    {TW_V2S(2, false), TW_V2S(4, false), TW_V2L(8, false), TW_V2XL(false)},
+    {TW_V2S(2, true), TW_V2S(4, true), TW_V2L(8, true), TW_V2XL(true)}};
 #undef TW_V2S
 #undef TW_V2L
+#undef TW_V2XL
 #define TW_V1(K, E) {fused_kernel<K, 1, 0, E>, fused_kernel<K, 1, 16, E>}
 const KernelFn kVpt1[2][5][2] = {
     {TW_V1(1, false), TW_V1(2, false), TW_V1(4, false), TW_V1(8, false), TW_V1(16, false)},
