@@ -324,7 +324,7 @@ def job_throughput(units_per_rank, elapsed_s_max, world):
 # ------------------------------------------------------------------ the GPU arm
 
 
-def make_sets(name, T_override, l2_bytes, device, N_override=0):
+def make_sets(name, T_override, l2_bytes, device, N_override=0, H_override=0):
     import torch
     import synth
     w = dict(synth.WORKLOADS[name])
@@ -332,6 +332,8 @@ def make_sets(name, T_override, l2_bytes, device, N_override=0):
         w["T"] = T_override
     if N_override:
         w["N"] = N_override
+    if H_override:
+        w["H"] = H_override
     T, H, N = w["T"], w["H"], w["N"]
     per_set = (N + 2) * T * H * 2 + H * 2  # resident bytes of one set (inputs + output)
     nsets = max(1, math.ceil(4 * l2_bytes / per_set))
@@ -878,7 +880,8 @@ def reference_arm(args, rank, world):
 
 def sweep(args):
     """GB/s and GB/s per SM for T = 512..16384 and budgets 2/4/8/16/full
-    (H=8192, N=8); one JSON line per cell. The headline figure per cell is the
+    (H=8192, N=8 unless --sweep-hidden / --sweep-partials say otherwise); one
+    JSON line per cell. The headline figure per cell is the
     median of per-launch CUDA events (launch latency included); b2b_us and
     graph_us are the mean per launch over the same launches issued back to
     back eagerly and replayed from one CUDA graph. All three launch prepared
@@ -894,8 +897,9 @@ def sweep(args):
     tokens = [int(t) for t in args.sweep_tokens.split(",")]
     budgets = [int(b) for b in args.sweep_budgets.split(",")]
     partials = [int(n) for n in args.sweep_partials.split(",")]
-    for T, Nsw in [(t, n) for t in tokens for n in partials]:
-        T_, H, N, sets, per_set = make_sets("llama70b_t1024_h8192_n8", T, l2, dev, Nsw)
+    hiddens = [int(h) for h in args.sweep_hidden.split(",")]
+    for T, Nsw, Hsw in [(t, n, h) for h in hiddens for t in tokens for n in partials]:
+        T_, H, N, sets, per_set = make_sets("llama70b_t1024_h8192_n8", T, l2, dev, Nsw, Hsw)
         bytes_call = tw.bytes_per_call(T, H, N)
         for budget in budgets:
             reps = args.sweep_reps
@@ -1194,6 +1198,7 @@ def main(argv=None):
     ap.add_argument("--sweep-budgets", default="2,4,8,16,0")
     ap.add_argument("--sweep-reps", type=int, default=50)
     ap.add_argument("--sweep-partials", default="8", help="N values for --sweep")
+    ap.add_argument("--sweep-hidden", default="8192", help="H values for --sweep")
     ap.add_argument("--corun", action="store_true")
     ap.add_argument("--corun-tokens", default="1024,2048,4096,8192")
     ap.add_argument("--corun-budgets", default="2,4,8,16,0")
