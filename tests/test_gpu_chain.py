@@ -84,6 +84,11 @@ CASES = [
     (256, 8192, 8, 4, 8, False),     # under an SM budget of 8
     (4096, 8192, 8, 3, 0, True),     # planned 2048/2048 split on two streams, per step
     (4864, 8192, 2, 3, 16, True),    # uneven planned split under a budget
+    (1024, 8192, 2, 5, 8, False),    # two-pipeline chunk ring (N <= 4, >= 4 rows per CTA)
+    (2048, 8192, 4, 4, 0, False),    # two-pipeline chunk ring on the whole GPU
+    (512, 6152, 3, 4, 8, False),     # two-pipeline chunk ring, ragged rows
+    (512, 8192, 12, 4, 8, False),    # two-pipeline row ring (N >= 9 under a budget)
+    (256, 8192, 16, 3, 4, False),    # two-pipeline row ring, compile-time N = 16
 ]
 
 
