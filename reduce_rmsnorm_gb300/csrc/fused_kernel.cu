@@ -27,13 +27,14 @@
 //     16-byte stores. The per-row arithmetic depends only on H, so every grid
 //     size (SM budget), split and shard gives bitwise the same rows.
 //   * L2 policy per call: evict-first loads and a streaming output when no
-//     CTA owns more than one row, for N <= 2 or N >= 9 with an output of at
-//     most an eighth of the L2, and for N <= 2 with an output of at least
-//     7/16 of it; otherwise the normal policy.
+//     CTA owns more than one row and that row is over 144 KiB, for N <= 2 or
+//     N >= 9 with an output of at most an eighth of the L2, and for N <= 2
+//     with an output of at least 7/16 of it; otherwise the normal policy.
 //   * Programmatic dependent launch: the CTAs set up their barriers while the
 //     previous kernel in the stream drains, ask L2 for the first ~144 KiB of
-//     their rows (a prefetch hint, when a CTA owns more than one row), then
-//     wait (griddepcontrol.wait) before reading or writing global memory.
+//     their rows (a prefetch hint, when a CTA owns more than one row or its
+//     one row fits in it), then wait (griddepcontrol.wait) before reading or
+//     writing global memory.
 //   * Every wait on an mbarrier is bounded (time and iterations); on giving up
 //     the CTA sets a device error word and finishes without further waits.
 #include <cuda_bf16.h>
@@ -965,22 +966,31 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
   // N <= 2 and N >= 9 while the output is at most an eighth of the L2 (+1-6%
   // at T <= 1024, H = 8192), and for N <= 2 again once the output reaches
   // 7/16 of the L2 (+1-3.5% at T = 4096-8192); in between, normal loads win
-  // by 2-5%. Without the prefetch (one row per CTA) evict-first wins for
-  // N = 4 and 8 at every shape measured (+2-10% at T = 32-152,
-  // H = 4096-16384).
+  // by 2-5%. With one row per CTA and no prefetch (a row over 144 KiB)
+  // evict-first wins for N = 4 and 8 at every shape measured (+2-10% at
+  // T = 32-152, H = 4096-16384); with the whole-row prefetch below, normal
+  // loads win for N = 3-8 (+1-6% at T = 32-128, H = 8192), and N <= 2 keeps
+  // evict-first through its small-output clause.
   const int64_t out_bytes = a.rows * a.hidden * 2;
   const int64_t l2 = static_cast<int64_t>(d->l2_bytes);
   const bool small_out = out_bytes * 8 <= l2;
   const bool large_out = out_bytes * 16 >= l2 * 7;
   const bool one_row_per_cta = a.rows <= shape.grid;
-  p.l2_stream = (one_row_per_cta || (a.n <= 2 && (small_out || large_out)) ||
+  const bool row_fits = static_cast<int64_t>(a.n + 1) * a.hidden * 2 <=
+                        static_cast<int64_t>(kPrefetchPerCta);
+  p.l2_stream = ((one_row_per_cta && !row_fits) || (a.n <= 2 && (small_out || large_out)) ||
                  (a.n >= 9 && small_out))
                     ? 1
                     : 0;
-  // About 144 KiB per CTA, shared among the N + 1 sources. Only when some CTA
-  // owns more than one row: with one row per CTA no CTA starts early.
-  p.prefetch_bytes = !one_row_per_cta ? (kPrefetchPerCta / static_cast<uint32_t>(a.n + 1)) & ~15u
-                                      : 0u;
+  // About 144 KiB per CTA, shared among the N + 1 sources. With one row per
+  // CTA only when that covers the whole row ((N + 1) * H * 2 <= 144 KiB): the
+  // next launch's CTAs land on SMs as this launch's one-row CTAs leave them,
+  // and a whole-row prefetch took 7-17% off back-to-back launches at
+  // T = 16-152 (H = 2048-8192 at every N; H = 16384 at N = 2), while a
+  // partial one (H = 16384, N = 8; H = 32768) measured up to 12% slower.
+  p.prefetch_bytes = (!one_row_per_cta || row_fits)
+                         ? (kPrefetchPerCta / static_cast<uint32_t>(a.n + 1)) & ~15u
+                         : 0u;
   p.rows = a.rows;
   p.vec_per_row = static_cast<int>(a.hidden / 8);
   p.n_partials = a.n;
