@@ -207,7 +207,7 @@ def _check_devices(where, tensors=(), streams=()):
     (ints) cannot be checked here."""
     dev = _current_device()
     for name, t in tensors:
-        if t is not None and t.device.index != dev:
+        if t is not None and t.get_device() != dev:
             raise ValueError("%s: %s is on %s but the current device is cuda:%d; all tensors "
                              "and streams must be on the current device" % (where, name, t.device,
                                                                             dev))

@@ -368,6 +368,9 @@ class _FakeCudaTensor:
     def data_ptr(self):
         return self._ptr
 
+    def get_device(self):
+        return self.device.index
+
 
 class _FakeStream:
     def __init__(self, index):
