@@ -215,6 +215,21 @@ __device__ bool drain_phase(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// Waits (bounded) until every bulk copy a producer issued into its ring of
+// `stages` stages has landed: `issued` items went out in order, item i on
+// stage i % stages in phase i / stages, so the last item of each stage
+// completes after all earlier ones there. The producer owns this drain, on
+// the normal path too (where it returns as the consumers' waits complete),
+// so no CTA exits with copies into its shared memory in flight, even if a
+// consumer gives up a wait after the producer has left its issue loop.
+__device__ void drain_ring(uint64_t* full, int stages, long long issued) {
+  const long long last = issued - 1;
+  for (int st = 0; st < stages && st <= last; ++st) {
+    const long long it_last = last - ((last - st) % stages);
+    drain_phase(&full[st], static_cast<uint32_t>((it_last / stages) & 1));
+  }
+}
+
 // ------------------------------------------------------------------ bf16 x 8
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -320,6 +335,38 @@ __device__ __forceinline__ void reduce_vector(uint32_t src, uint32_t cbytes, int
   }
 }
 
+// The end of a row, shared by both kernel forms: the sum of squares is
+// reduced across the warp (xor shuffle) and then across the pipeline's 8
+// warps in warp order (through `wsum`, this row's 8 floats), r = rsqrt(mean +
+// eps), and Y = (z * r) * gamma is stored as bf16. With evict-first loads the
+// output is stored streaming too, so its lines drain during this launch; with
+// normal loads the store policy measured within 0.2%. A kernel that reads Y
+// right after still finds it unless L2 needs the room. The residual keeps the
+// default policy (evict-first there measured -1%).
+template <int KMAX, bool EXACT, int GN>
+__device__ __forceinline__ void finish_row(const Params& p, float ss, const float (&z)[KMAX][8],
+                                           const uint4 (&g_reg)[GN], float* wsum, int bar_id,
+                                           int lane, int wg, int t, int vpr, long long row) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) wsum[wg] = ss;
+  asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "n"(kConsumerThreads) : "memory");
+  const float total = warp_total(wsum);
+  const float rs = rsqrtf(total / p.hidden + p.eps);
+  uint4* out_row = p.out + row * vpr;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    const int v = j * kSlotVec + t;
+    if (EXACT || v < vpr) {
+      float y[8];
+      if constexpr (GN == KMAX) scale8(z[j], rs, g_reg[j], y);
+      else scale8(z[j], rs, __ldg(p.gamma + v), y);
+      if (p.l2_stream) __stcs(out_row + v, pack8(y));
+      else out_row[v] = pack8(y);
+    }
+  }
+}
+
 // KMAX:  slots of a row held in registers (ceil(H/8 / 256) rounded up to a
 //        power of two, >= VPT).
 // VPT:   slots per chunk (1: 4 KiB copies; 2: 8 KiB copies).
@@ -363,13 +410,14 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   // rows of pipeline g: [part(g), part(g + 1))
   auto part = [&](int g) { return row0 + (row1 - row0) * g / G; };
 
-  // thread s sets up stage s's two barriers
-  if (tid < G * stages) {
-    mbar_init(&full_bar[tid], 1);
-    mbar_init(&empty_bar[tid], kConsumerWarps);
+  if (tid == 0) {
+    for (int s = 0; s < G * stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid == 0) abort_flag = 0;
   __syncthreads();
   // Producer lane -> (pipeline, source): lane r for G = 1; lane 16 g + r for
   // G = 2.
@@ -439,19 +487,7 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
       if (++chunk == chunks) { chunk = 0; ++row; }
       if (++s == stages) { s = 0; round_parity ^= 1u; first_pass = false; }
     }
-    if (src_lane == 0) {
-      // The producer owns the drain: every copy this CTA issued lands before
-      // the CTA can exit, whether or not a consumer gave up a wait (possibly
-      // after the producer left its loop). The last item issued on each stage
-      // completes after all earlier ones there. On the normal path the
-      // consumers have waited for (or will wait for) the same phases, so this
-      // returns as they complete.
-      const long long last = issued - 1;
-      for (int st = 0; st < stages && st <= last; ++st) {
-        const long long it_last = last - ((last - st) % stages);
-        drain_phase(&full[st], static_cast<uint32_t>((it_last / stages) & 1));
-      }
-    }
+    if (src_lane == 0) drain_ring(full, stages, issued);
     return;
   }
 
@@ -507,31 +543,10 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
         if (++s == stages) { s = 0; parity ^= 1u; }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const int buf = static_cast<int>((row - ra) & 1);
-    if (lane == 0) warp_ss[g][buf][wg] = ss;
-    asm volatile("bar.sync %0, %1;" ::"r"(kConsumerBarrierId + g), "n"(kConsumerThreads)
-                 : "memory");
-    const float total = warp_total(warp_ss[g][buf]);
-    const float rs = rsqrtf(total / p.hidden + p.eps);
-    uint4* out_row = p.out + row * vpr;
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      const int v = j * kSlotVec + t;
-      if (EXACT || v < vpr) {
-        float y[8];
-        if constexpr (kGammaRegs) scale8(z[j], rs, g_reg[j], y);
-        else scale8(z[j], rs, __ldg(p.gamma + v), y);
-        // With evict-first loads the output is stored streaming too, so its
-        // lines drain during this launch; with normal loads the store policy
-        // measured within 0.2%. A kernel that reads Y right after still finds
-        // it unless L2 needs the room. The residual keeps the default policy
-        // (evict-first there measured -1%).
-        if (p.l2_stream) __stcs(out_row + v, pack8(y));
-        else out_row[v] = pack8(y);
-      }
-    }
+    // the two row buffers of warp sums alternate, so a warp can post row i + 1
+    // while slower warps still read row i's
+    finish_row<KMAX, EXACT>(p, ss, z, g_reg, warp_ss[g][(row - ra) & 1], kConsumerBarrierId + g,
+                            lane, wg, t, vpr, row);
   }
 }
 
@@ -570,13 +585,14 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   // rows of pipeline g: [part(g), part(g + 1))
   auto part = [&](int g) { return row0 + (row1 - row0) * g / G; };
 
-  // thread s sets up stage s's two barriers
-  if (tid < G * spp) {
-    mbar_init(&full_bar[tid], 1);
-    mbar_init(&empty_bar[tid], kConsumerWarps);
+  if (tid == 0) {
+    for (int s = 0; s < G * spp; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid == 0) abort_flag = 0;
   __syncthreads();
   // L2 warm-up before the dependency wait, as in fused_kernel: lane r asks for
   // the first bytes of source r's rows of each pipeline.
@@ -627,13 +643,7 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
       if (++r > n) { r = 0; ++row; }
       if (++s == spp) { s = 0; round_parity ^= 1u; first_pass = false; }
     }
-    // The producer owns the drain (see fused_kernel): every copy it issued
-    // lands before the CTA can exit.
-    const long long last = issued - 1;
-    for (int st = 0; st < spp && st <= last; ++st) {
-      const long long it_last = last - ((last - st) % spp);
-      drain_phase(&full[st], static_cast<uint32_t>((it_last / spp) & 1));
-    }
+    drain_ring(full, spp, issued);
     return;
   }
 
@@ -701,26 +711,8 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
         res_row[v] = pack8(z[j]);
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const int buf = static_cast<int>((row - ra) & 1);
-    if (lane == 0) warp_ss[g][buf][wg] = ss;
-    asm volatile("bar.sync %0, %1;" ::"r"(kConsumerBarrierId + g), "n"(kConsumerThreads)
-                 : "memory");
-    const float total = warp_total(warp_ss[g][buf]);
-    const float rs = rsqrtf(total / p.hidden + p.eps);
-    uint4* out_row = p.out + row * vpr;
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      const int v = j * kSlotVec + t;
-      if (EXACT || v < vpr) {
-        float y[8];
-        if constexpr (kGammaRegs) scale8(z[j], rs, g_reg[j], y);
-        else scale8(z[j], rs, __ldg(p.gamma + v), y);
-        if (p.l2_stream) __stcs(out_row + v, pack8(y));
-        else out_row[v] = pack8(y);
-      }
-    }
+    finish_row<KMAX, EXACT>(p, ss, z, g_reg, warp_ss[g][(row - ra) & 1], kConsumerBarrierId + g,
+                            lane, wg, t, vpr, row);
   }
 }
 
