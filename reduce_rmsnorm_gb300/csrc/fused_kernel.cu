@@ -26,6 +26,13 @@
 //     combine of the 8 warp sums, rsqrtf, and Y = (z * r) * gamma stored with
 //     16-byte stores. The per-row arithmetic depends only on H, so every grid
 //     size (SM budget), split and shard gives bitwise the same rows.
+//   * Two more forms serve an SM budget, where each SM must stream as much as
+//     it can: two independent pipelines per CTA (each its own producer lanes,
+//     half of the ring and 8 consumer warps) for N <= 4, where the consumers'
+//     work per byte caps an SM; and the row ring (rowring_kernel), one bulk
+//     copy per source row, for N >= 9, where 4 KiB copies cap it. Each thread
+//     owns the same vectors and adds in the same order in every form, so the
+//     forms give bitwise the same rows; select_kernel picks one by speed.
 //   * L2 policy per call: evict-first loads and a streaming output when no
 //     CTA owns more than one row and that row is over 144 KiB, for N <= 2 or
 //     N >= 9 with an output of at most an eighth of the L2, and for N <= 2
