@@ -401,7 +401,8 @@ def after_gemm(tw, sets, eps, stream, H, N, reps=30):
 def compact_sweep(tw, dev, l2, peak, reps=20):
     """The rest of the metric in the default line: GB/s and tokens/s at
     T = 1024 / 4096 / 16384 on the whole GPU, and GB/s per SM at SM budgets
-    2 / 4 / 8 / 16 for T = 8192 (H = 8192, N = 8). Inputs are made on the
+    2 / 4 / 8 / 16 for T = 8192 (H = 8192, N = 8), plus N = 2 and N = 12 at
+    an 8-SM budget (T = 4096). Inputs are made on the
     device from a seeded generator with the workload's distributions (this
     measures time only; parity runs on the synthetic CPU inputs). Each cell
     times `reps` prepared launches back to back between one event pair, and
@@ -409,10 +410,10 @@ def compact_sweep(tw, dev, l2, peak, reps=20):
     rotate over enough sets to exceed 4x the L2, or one set is already larger
     than that."""
     import torch
-    H, N, eps = 8192, 8, 1e-5
+    H, eps = 8192, 1e-5
     gen = torch.Generator(device=dev).manual_seed(0)
 
-    def make(T):
+    def make(T, N):
         per_set = (N + 2) * T * H * 2
         out = []
         for _ in range(max(1, math.ceil(4 * l2 / per_set))):
@@ -427,7 +428,7 @@ def compact_sweep(tw, dev, l2, peak, reps=20):
     stream = torch.cuda.Stream(dev)
     stream.wait_stream(torch.cuda.current_stream(dev))
 
-    def cell(sets, T, budget):
+    def cell(sets, T, N, budget):
         calls = [tw.FusedCall(s["P"], s["R"], s["G"], eps, s["out"], stream=stream,
                               sm_budget=budget) for s in sets]
         with torch.cuda.stream(stream):
@@ -450,23 +451,25 @@ def compact_sweep(tw, dev, l2, peak, reps=20):
         nbytes = tw.bytes_per_call(T, H, N)
         used = tw.tw_launch_shape(T, H, N, budget)["grid"]
         gbs = nbytes / b2b / 1e3
-        return {"T": T, "sm_budget": budget or "full", "sms_used": used,
+        return {"T": T, "N": N, "sm_budget": budget or "full", "sms_used": used,
                 "us_b2b": round(b2b, 2), "GB_s": round(gbs, 1), "frac": round(gbs / peak, 4),
                 "GB_s_per_sm": round(gbs / used, 2), "tokens_per_s": round(T / b2b * 1e6, 1),
                 "us_per_launch": round(per, 2),
                 "GB_s_per_launch": round(nbytes / per / 1e3, 1)}
 
     cells = []
-    for T, budgets in ((1024, (0,)), (4096, (0,)), (16384, (0,)), (8192, (2, 4, 8, 16, 0))):
-        sets = make(T)
+    # N = 8 over T and budgets; N = 2 and 12 under an 8-SM budget, where the
+    # launch takes the two-pipeline forms
+    for T, N, budgets in ((1024, 8, (0,)), (4096, 8, (0,)), (16384, 8, (0,)),
+                          (8192, 8, (2, 4, 8, 16, 0)), (4096, 2, (8,)), (4096, 12, (8,))):
+        sets = make(T, N)
         torch.cuda.synchronize()
         for budget in budgets:
-            # budgeted launches are long (ms): fewer reps keep the block short
-            cells.append(cell(sets, T, budget))
+            cells.append(cell(sets, T, N, budget))
         del sets
     torch.cuda.current_stream(dev).wait_stream(stream)
     torch.cuda.empty_cache()
-    return {"H": H, "N": N, "reps": reps, "cells": cells,
+    return {"H": H, "reps": reps, "cells": cells,
             "timing": "us_b2b: launches back to back between one event pair (GB_s, frac, "
                       "GB_s_per_sm, tokens_per_s); us_per_launch: median of an event pair "
                       "around each launch (launch latency included)"}
