@@ -89,8 +89,10 @@ def _one_case_per_instance():
 @pytest.mark.parametrize("T,budget", [(3, 0), (40, 3)])
 @pytest.mark.parametrize("H,N", _one_case_per_instance())
 def test_parity_every_kernel_instance(H, N, T, budget):
-    """T=3: one row per CTA (no L2 prefetch); T=40 on 3 SMs: 13-14 rows per
-    CTA, so the ring wraps across rows and the prefetch is issued."""
+    """T=3: one row per CTA (the L2 prefetch is issued when the row fits in
+    144 KiB); T=40 on 3 SMs: 13-14 rows per CTA, so the ring wraps across
+    rows, the prefetch is issued, and KMAX = 4 shapes take the two-pipeline
+    forms."""
     p, r, g = synth.make_inputs(T, H, N, 0.02, seed=H + N + T)
     R, out = run(p, r, g, sm_budget=budget)
     check_rows(p, r, g, EPS, R, out)
@@ -418,11 +420,18 @@ def test_split_same_stream():
     assert_same(ref[1], out)
 
 
+@pytest.mark.parametrize("N", [8, 2, 12])
 @pytest.mark.parametrize("budget", [1, 2, 4, 8, 16])
-def test_sm_budget_occupies_at_most_budget_sms(budget):
-    T, H, N = 512, 8192, 8
+def test_sm_budget_occupies_at_most_budget_sms(budget, N):
+    """N = 8 takes the one-pipeline chunk ring, N = 2 the two-pipeline chunk
+    ring and N = 12 the two-pipeline row ring: every form must keep one CTA
+    per SM (more than half an SM's shared memory) so that a budget of k CTAs
+    occupies at most k SMs."""
+    T, H = 512, 8192
     shape = tw.tw_launch_shape(T, H, N, budget)
     assert shape["grid"] == min(budget, T)
+    assert shape["smem_bytes"] > 114 * 1024
+    assert shape["threads"] == (288 if N == 8 else 544)
     p, r, g = synth.make_inputs(T, H, N, 0.02, seed=2)
     P, R, G = to_gpu(p, r, g)
     out = torch.empty_like(R)
