@@ -536,12 +536,50 @@ def test_parity_random_shapes(T, H, N, budget):
     check_rows(p, r, g, EPS, R, out)
 
 
-@pytest.mark.parametrize("which,budget,split", [(0, 0, False), (7, 0, False), (3, 4, False),
-                                                 (0, 0, True)])
-def test_output_written_over_a_partial(which, budget, split):
+def _random_two_pipeline_shapes(count, seed):
+    """Shapes that take the two-pipeline forms: H/8 in 513..1024 with
+    N = 1..4 (the chunk ring; ragged H only up to N = 3), or H = 8192 with
+    N = 9..16 (the row ring), under budgets where every CTA owns >= 4 rows."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shapes = []
+    while len(shapes) < count:
+        budget = int(rng.choice([2, 3, 5, 8]))
+        if rng.random() < 0.5:
+            N = int(rng.integers(1, 5))
+            H = 8 * int(rng.integers(513, 1025)) if N <= 3 else 8192
+        else:
+            N, H = int(rng.integers(9, 17)), 8192
+        T = int(rng.integers(4 * budget, 4 * budget + 60))
+        if T * H * (N + 1) > 8_000_000:     # keep the oracle to seconds
+            continue
+        shapes.append((T, H, N, budget))
+    return shapes
+
+
+@pytest.mark.parametrize("T,H,N,budget", _random_two_pipeline_shapes(16, 77))
+def test_parity_random_two_pipeline_shapes(T, H, N, budget):
+    """Seeded random shapes in the two-pipeline forms, every row checked
+    against the oracle, and bitwise equal to the whole-GPU launch of the same
+    rows: a one-pipeline chunk ring for the N <= 4 shapes (whose CTAs then
+    own under 4 rows), the row ring on another grid for the N >= 9 shapes."""
+    shape = tw.tw_launch_shape(T, H, N, budget)
+    assert shape["threads"] == 544, (T, H, N, budget, shape)
+    p, r, g = synth.make_inputs(T, H, N, 0.03, seed=T + H + N + budget)
+    R, out = run(p, r, g, sm_budget=budget)
+    check_rows(p, r, g, EPS, R, out)
+    R1, out1 = run(p, r, g, sm_budget=0)
+    assert_same(R, R1)
+    assert_same(out, out1)
+
+
+@pytest.mark.parametrize("which,budget,split,N", [(0, 0, False, 8), (7, 0, False, 8),
+                                                   (3, 4, False, 8), (0, 0, True, 8),
+                                                   (1, 8, False, 2), (11, 8, False, 12)])
+def test_output_written_over_a_partial(which, budget, split, N):
     """out == partials[r]: Y written over one rank's partial equals the result
-    into a separate buffer, bit for bit (also under an SM budget and split)."""
-    T, H, N = 2048, 8192, 8
+    into a separate buffer, bit for bit (also under an SM budget and split,
+    and in the two-pipeline chunk ring (N=2) and row ring (N=12))."""
+    T, H = 2048, 8192
     p, r, g = synth.make_inputs(T, H, N, 0.02, seed=91)
     ref = run(p, r, g, sm_budget=budget)
     P, R, G = to_gpu(p, r, g)
