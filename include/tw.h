@@ -97,11 +97,14 @@ typedef enum {
  *              partial; no other overlap with an input is allowed.
  *   stream     the stream to launch on.
  *   sm_budget  0: use the whole GPU (one CTA per SM). k > 0: launch at most k
- *              CTAs, each owning one SM (it requests enough shared memory that
- *              no second CTA of this kernel fits) and a contiguous range of
- *              about T / k rows, so the step co-runs with work on the other
- *              SMs ([W] "What it buys": 2 to 8 SMs). k above the SM count is
- *              clamped. Negative is invalid.
+ *              CTAs, each owning a contiguous range of about T / k rows, so
+ *              the step occupies at most k SMs and co-runs with work on the
+ *              other SMs ([W] "What it buys": 2 to 8 SMs). A CTA that owns
+ *              more than one row requests enough shared memory that no second
+ *              CTA of this kernel fits on its SM; with one row per CTA (T <= k
+ *              or T <= the SM count) it requests only that row's staging, so
+ *              small rows may share an SM with the next launch's CTAs. k above
+ *              the SM count is clamped. Negative is invalid.
  *
  * Errors: TW_ERR_INVALID_ARG (N, T, H <= 0, eps, sm_budget, a null pointer,
  * residual/out overlapping each other or any input other than out ==

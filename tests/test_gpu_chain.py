@@ -81,6 +81,7 @@ CASES = [
     (1024, 8192, 8, 6, 0, False),    # the Llama-3.3-70B layer shape
     (333, 4104, 3, 5, 0, False),     # ragged rows and chunks, runtime N
     (128, 4096, 2, 8, 0, False),     # the PR1 shape: one row per CTA
+    (152, 4096, 8, 6, 0, False),     # one row per CTA on every SM, a one-stage 72 KiB ring
     (256, 8192, 8, 4, 8, False),     # under an SM budget of 8
     (4096, 8192, 8, 3, 0, True),     # planned 2048/2048 split on two streams, per step
     (4864, 8192, 2, 3, 16, True),    # uneven planned split under a budget
