@@ -16,7 +16,10 @@
  *     size, which sets the per-call L2 policy).
  *   - Launches are asynchronous on the stream(s) given; a device fault shows
  *     at the caller's next synchronisation, as usual in CUDA. Work runs on the
- *     device that is current on the calling thread.
+ *     device that is current on the calling thread, and every pointer and
+ *     stream must belong to that device. libtw does not check this (a query
+ *     per pointer would cost more host time than a small step's launch); the
+ *     Python binding refuses tensors and streams on other devices.
  *   - Every launch uses programmatic dependent launch: its thread blocks may
  *     become resident while the previous kernel on the stream is still
  *     running. The fused step's blocks then ask L2 to prefetch the first bytes

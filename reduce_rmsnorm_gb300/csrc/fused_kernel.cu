@@ -403,6 +403,8 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   constexpr uint32_t kChunkBytes = kSlotBytes * VPT;
   constexpr int kProducerWarp = G * kConsumerWarps;
   static_assert(KMAX % VPT == 0, "slots must fill whole chunks");
+  // G = 2 is instantiated only with a compile-time N of 1..4 (kChunkTwo): each
+  // pipeline's producer group is lanes 16 g .. 16 g + N.
   static_assert(G == 1 || NT <= 15, "two pipelines take at most 16 producer lanes each");
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
