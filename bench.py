@@ -20,7 +20,11 @@ Rank 0 prints ONE JSON line. ``value`` is whole-job algorithmic GB/s:
 (N+3)*T*H*2 + H*2 bytes per step, times the steps of all ranks, over the
 slowest rank's device time. With torchrun (N>1) every rank runs its own
 replica of the workload (the step has no cross-GPU exchange on one node's
-replicas), and the timing is the max over ranks.
+replicas), and the timing is the max over ranks. Besides the timed region the
+line carries the step timed per launch and right after the row-parallel GEMM
+(``roofline``), a compact sweep over T and SM budgets (``sweep``), the
+unfused baseline, the end-to-end leg from host buffers (``e2e``) and the CPU
+oracle (``cpu_baseline``).
 """
 
 import argparse
