@@ -93,7 +93,10 @@ struct Params {
   int vec_per_row;  // H / 8
   int n_partials;
   int chunks;       // ceil(vec_per_row / (kSlotVec * VPT))
-  int stages;
+  int stages;       // stages of the ring (of pipeline 0 with two pipelines)
+  int stages1;      // two pipelines: pipeline 1's stages
+  int split_num;    // two pipelines: pipeline 0 owns split_num / split_den of the
+  int split_den;    // CTA's rows
   float eps;
   float hidden;
 };
@@ -415,13 +418,17 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   const int n = NT > 0 ? NT : p.n_partials;
   const int vpr = EXACT ? KMAX * kSlotVec : p.vec_per_row;
   const int chunks = EXACT ? KMAX / VPT : p.chunks;
-  const int stages = p.stages;  // of each pipeline
+  const int st0 = p.stages, st1 = G == 1 ? 0 : p.stages1;  // stages of pipelines 0 and 1
   const uint32_t stage_bytes = static_cast<uint32_t>(n + 1) * kChunkBytes;
-  // rows of pipeline g: [part(g), part(g + 1))
-  auto part = [&](int g) { return row0 + (row1 - row0) * g / G; };
+  // rows of pipeline g: [part(g), part(g + 1)); pipeline 0 owns split_num /
+  // split_den of the CTA's rows (half, or more when its ring is deeper)
+  auto part = [&](int g) {
+    if constexpr (G == 1) return row0 + (row1 - row0) * g;
+    else return g == 0 ? row0 : (g == G ? row1 : row0 + (row1 - row0) * p.split_num / p.split_den);
+  };
 
   if (tid == 0) {
-    for (int s = 0; s < G * stages; ++s) {
+    for (int s = 0; s < st0 + st1; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kConsumerWarps);
     }
@@ -467,9 +474,11 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
     if (src_lane > n || pg >= G) return;
     const unsigned lanes = (n + 1 == 32 ? 0xffffffffu : ((1u << (n + 1)) - 1u)) << (16 * pg);
     const int lead = 16 * pg;  // the pipeline's first lane
-    uint64_t* full = full_bar + pg * stages;
-    uint64_t* empty = empty_bar + pg * stages;
-    unsigned char* my_ring = ring + static_cast<size_t>(pg) * stages * stage_bytes;
+    const int stages = (G == 1 || pg == 0) ? st0 : st1;
+    const int first = pg == 0 ? 0 : st0;  // the pipeline's first stage
+    uint64_t* full = full_bar + first;
+    uint64_t* empty = empty_bar + first;
+    unsigned char* my_ring = ring + static_cast<size_t>(first) * stage_bytes;
     // Evict-first or normal L2 policy for the loads, chosen per call on the
     // host (launch_fused).
     const uint64_t policy = p.l2_stream ? l2_evict_first_policy() : l2_evict_normal_policy();
@@ -506,9 +515,11 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   const int g = warp / kConsumerWarps;
   const int wg = warp % kConsumerWarps;
   const int t = tid - g * kConsumerThreads;
-  uint64_t* full = full_bar + g * stages;
-  uint64_t* empty = empty_bar + g * stages;
-  const uint32_t ring_base = smem_addr(ring) + static_cast<uint32_t>(g * stages) * stage_bytes +
+  const int stages = (G == 1 || g == 0) ? st0 : st1;
+  const int first = G == 1 ? g * st0 : (g == 0 ? 0 : st0);  // the pipeline's first stage
+  uint64_t* full = full_bar + first;
+  uint64_t* empty = empty_bar + first;
+  const uint32_t ring_base = smem_addr(ring) + static_cast<uint32_t>(first) * stage_bytes +
                              static_cast<uint32_t>(t) * 16u;
   // gamma stays in registers for the CTA's whole row range (read once per CTA)
   constexpr bool kGammaRegs = KMAX <= 8;
@@ -796,6 +807,8 @@ struct Choice {
   int rowring;  // 0: chunk ring (fused_kernel); 1: row ring (rowring_kernel)
   int groups;   // pipelines per CTA
   int vpt;      // chunk ring: slots per chunk
+  int stages1;  // set by shape_for: two pipelines, pipeline 1's stages
+  int split_num, split_den;  // set by shape_for: pipeline 0's share of the rows
 };
 
 // Per-device attributes, queried once; the launch path reads them without a
@@ -925,6 +938,22 @@ int shape_for(const DeviceInfo& d, int64_t rows, int64_t hidden, int n, int sm_b
   int stages = (d.smem_optin - kStaticSmemReserve) / (c.groups * stage_bytes);
   if (stages > kMaxStages / c.groups) stages = kMaxStages / c.groups;
   if (stages < 2) return TW_ERR_UNSUPPORTED;
+  Choice cc = c;
+  cc.stages1 = c.groups == 2 ? stages : 0;
+  cc.split_num = 1;
+  cc.split_den = 2;
+  const int whole = (d.smem_optin - kStaticSmemReserve) / stage_bytes;  // stages of one ring
+  if (c.groups == 2 && !c.rowring && stages == 2 && whole >= 5 && 2 * grid <= d.sms) {
+    // Two chunk-ring pipelines of 2 stages each (N = 4 at 40 KiB a stage)
+    // leave a fifth stage unused. Under an SM budget pipeline 0 takes it and
+    // 13/20 of the rows: 107-110 -> 115-117 GB/s per SM at 2-16 SMs (shares
+    // of 11/20, 3/5 and 7/10 measured 110-111, 113-116, 114-117). On the
+    // whole GPU the even split was 1-2% faster.
+    stages = 3;
+    cc.stages1 = 2;
+    cc.split_num = 13;
+    cc.split_den = 20;
+  }
   if (rows <= grid && !c.rowring && c.groups == 1) {
     // One row per CTA: a ring of the row's chunks holds the whole row. Where
     // that is under half an SM's shared memory (H <= 4096; H = 8192 with
@@ -937,10 +966,10 @@ int shape_for(const DeviceInfo& d, int64_t rows, int64_t hidden, int n, int sm_b
   }
   shape->grid = grid;
   shape->threads = c.groups * kConsumerThreads + 32;
-  shape->smem_bytes = stages * stage_bytes * c.groups;
+  shape->smem_bytes = (stages + cc.stages1) * stage_bytes;
   shape->stages = stages;
   shape->kmax = c.kmax;
-  *choice = c;
+  *choice = cc;
   return TW_OK;
 }
 
@@ -1009,6 +1038,9 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
   const int chunk_vec = kSlotVec * (choice.rowring ? 1 : choice.vpt);  // row ring: unused
   p.chunks = (p.vec_per_row + chunk_vec - 1) / chunk_vec;
   p.stages = shape.stages;
+  p.stages1 = choice.stages1;
+  p.split_num = choice.split_num;
+  p.split_den = choice.split_den;
   p.eps = a.eps;
   p.hidden = static_cast<float>(a.hidden);
 
