@@ -857,10 +857,12 @@ int vpt_for(int n) { return n <= 8 ? 2 : 1; }
 //    Per SM at an 8-SM budget (T = 4096) N = 1 78 -> 102 GB/s, 2: 88 -> 116,
 //    3: 98 -> 121, 4: 107 -> 108; at full GPU 0-5% faster for T >= 1024, but
 //    6% slower with ~3 rows per CTA (T = 512, N = 4), hence the row floor.
-//  * N >= 9, whole-chunk rows, a grid of at most half the SMs: the row ring
-//    with two pipelines, whose 16 KiB copies lift the per-SM rate from 83-95
-//    to 112 GB/s at an 8-SM budget. At full GPU, where an SM needs ~45 GB/s,
-//    the chunk ring is 2-4% faster.
+//  * N >= 9, whole-chunk rows, a grid of at most half the SMs, more rows than
+//    CTAs: the row ring with two pipelines, whose 16 KiB copies lift the
+//    per-SM rate from 83-95 to 112 GB/s at an 8-SM budget. At full GPU, where
+//    an SM needs ~45 GB/s, the chunk ring is 2-4% faster. With one row per
+//    CTA one of the two pipelines idles and the chunk ring, with every
+//    source's chunks in flight, is 10-20% faster (T = 16-76, N = 9-16).
 //  * otherwise the chunk ring with one pipeline.
 Choice select_kernel(int vpr, int n, int64_t rows, int grid, int sms) {
   Choice c;
@@ -879,7 +881,7 @@ Choice select_kernel(int vpr, int n, int64_t rows, int grid, int sms) {
     c.fn = kChunkTwo[exact][n - 1];
     return c;
   }
-  if (n >= 9 && vpr == 4 * kSlotVec && 2 * grid <= sms) {
+  if (n >= 9 && vpr == 4 * kSlotVec && 2 * grid <= sms && rows > grid) {
     c.rowring = 1;
     c.groups = 2;
     c.kmax = 4;

@@ -560,16 +560,36 @@ def _random_two_pipeline_shapes(count, seed):
 def test_parity_random_two_pipeline_shapes(T, H, N, budget):
     """Seeded random shapes in the two-pipeline forms, every row checked
     against the oracle, and bitwise equal to the whole-GPU launch of the same
-    rows: a one-pipeline chunk ring for the N <= 4 shapes (whose CTAs then
-    own under 4 rows), the row ring on another grid for the N >= 9 shapes."""
+    rows, which takes the one-pipeline chunk ring (its CTAs own under 4 rows,
+    or one row each)."""
     shape = tw.tw_launch_shape(T, H, N, budget)
     assert shape["threads"] == 544, (T, H, N, budget, shape)
+    assert tw.tw_launch_shape(T, H, N, 0)["threads"] == 288
     p, r, g = synth.make_inputs(T, H, N, 0.03, seed=T + H + N + budget)
     R, out = run(p, r, g, sm_budget=budget)
     check_rows(p, r, g, EPS, R, out)
     R1, out1 = run(p, r, g, sm_budget=0)
     assert_same(R, R1)
     assert_same(out, out1)
+
+
+@pytest.mark.parametrize("T", [1, 16, 76])
+@pytest.mark.parametrize("N", [9, 16])
+def test_one_row_per_cta_takes_the_chunk_ring(T, N):
+    """N >= 9 at H = 8192 with one row per CTA: the one-pipeline chunk ring,
+    with every source's chunks in flight, rather than the two-pipeline row
+    ring (one of whose pipelines would idle). Every row against the oracle, and
+    bitwise equal to a 4-SM budget launch (the row ring once a CTA owns more
+    than one row)."""
+    H = 8192
+    assert tw.tw_launch_shape(T, H, N, 0)["threads"] == 288
+    assert tw.tw_launch_shape(T, H, N, 4)["threads"] == (288 if T <= 4 else 544)
+    p, r, g = synth.make_inputs(T, H, N, 0.02, seed=7 * T + N)
+    R, out = run(p, r, g)
+    check_rows(p, r, g, EPS, R, out)
+    R4, out4 = run(p, r, g, sm_budget=4)
+    assert_same(R, R4)
+    assert_same(out, out4)
 
 
 @pytest.mark.parametrize("which,budget,split,N", [(0, 0, False, 8), (7, 0, False, 8),
