@@ -23,7 +23,8 @@ replica of the workload (the step has no cross-GPU exchange on one node's
 replicas), and the timing is the max over ranks. Besides the timed region the
 line carries the step timed per launch and right after the row-parallel GEMM
 (``roofline``), a compact sweep over T and SM budgets (``sweep``), the
-unfused baseline, the end-to-end leg from host buffers (``e2e``) and the CPU
+unfused baseline, the end-to-end leg from host buffers (``e2e``, with the
+same copies timed without the step as its host-link bound) and the CPU
 oracle (``cpu_baseline``).
 """
 
@@ -730,13 +731,43 @@ def e2e_arm(args, tw, T, H, N, eps, C, dev, sa, sb):
     e.record(s_h2d)
     torch.cuda.synchronize()
     ms = a.elapsed_time(e) / steps
+
+    def copies_only(k):
+        # the same transfers in the same pipeline, without the fused step
+        b = bufs[k % 2]
+        s_h2d.wait_event(b["drained"])
+        with torch.cuda.stream(s_h2d):
+            b["P"].copy_(hp, non_blocking=True)
+            b["R"].copy_(hr, non_blocking=True)
+            b["G"].copy_(hg, non_blocking=True)
+            b["loaded"].record(s_h2d)
+        s_d2h.wait_event(b["loaded"])
+        with torch.cuda.stream(s_d2h):
+            hr_out.copy_(b["R"], non_blocking=True)
+            hy_out.copy_(b["out"], non_blocking=True)
+            b["drained"].record(s_d2h)
+
+    for k in range(3):
+        copies_only(k)
+    torch.cuda.synchronize()
+    a.record(s_h2d)
+    for k in range(steps):
+        copies_only(k)
+    s_h2d.wait_stream(s_d2h)
+    e.record(s_h2d)
+    torch.cuda.synchronize()
+    link_ms = a.elapsed_time(e) / steps
     h2d = (N + 1) * T * H * 2 + H * 2
     d2h = 2 * T * H * 2
     return {"value": round(tw.bytes_per_call(T, H, N) / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(ms, 4),
             "pipeline": "2 device buffer sets; H2D, compute and D2H on separate streams",
-            "h2d_GB_s": round(h2d / (ms / 1e3) / 1e9, 1)}
+            "h2d_GB_s": round(h2d / (ms / 1e3) / 1e9, 1),
+            "link_bound": {"ms_per_step": round(link_ms, 4),
+                           "GB_s": round(tw.bytes_per_call(T, H, N) / (link_ms / 1e3) / 1e9, 2),
+                           "frac": round(link_ms / ms, 4),
+                           "what": "the same copies in the same pipeline without the fused step"}}
 
 
 # ------------------------------------------------------------------ the CPU oracle
