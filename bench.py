@@ -5,6 +5,7 @@
     python bench.py --sweep                   # SM-budget x token-count table (many lines)
     python bench.py --corun                   # split pipelined against a GEMM (many lines)
     python bench.py --offset-sweep [--sm-budget k]   # timed offset sweep -> lookup table
+    python bench.py --link                    # host-link copy bandwidth (e2e bytes)
 
 A step is one pass of the hot path over one batch: the wave-aware split plan
 and the fused step over the batch, prefix on one stream, suffix on another
@@ -1213,6 +1214,70 @@ def offset_sweep(args):
     assert tw.tw_device_status(reset=True) == 0
 
 
+# ------------------------------------------------------------------ host link
+
+
+def link_probe(args):
+    """Copy-engine bandwidth of the host link for the e2e leg's byte counts at
+    the workload's shape: host->device of the inputs, device->host of the two
+    outputs, and both at once, each on 1, 2 and 4 streams. One JSON line per
+    measurement."""
+    import torch
+    import synth
+    w = dict(synth.WORKLOADS[args.workload])
+    if args.tokens:
+        w["T"] = args.tokens
+    T, H, N = w["T"], w["H"], w["N"]
+    dev = torch.device("cuda", 0)
+    n_in = (N + 1) * T * H * 2 + H * 2
+    n_out = 2 * T * H * 2
+    h_in = torch.ones(n_in, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(n_out, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(n_in, dtype=torch.uint8, device=dev)
+    d_out = torch.zeros(n_out, dtype=torch.uint8, device=dev)
+    streams = [torch.cuda.Stream(dev) for _ in range(8)]
+    cur = torch.cuda.current_stream(dev)
+
+    def pieces(n, k):
+        step = -(-n // k)
+        return [(i * step, min(n, (i + 1) * step)) for i in range(k)]
+
+    def run(k, up, down):
+        for i in range(k):
+            if up:
+                s = streams[i]
+                s.wait_stream(cur)
+                a, b = pieces(n_in, k)[i]
+                with torch.cuda.stream(s):
+                    d_in[a:b].copy_(h_in[a:b], non_blocking=True)
+            if down:
+                s = streams[4 + i]
+                s.wait_stream(cur)
+                a, b = pieces(n_out, k)[i]
+                with torch.cuda.stream(s):
+                    h_out[a:b].copy_(d_out[a:b], non_blocking=True)
+        for s in streams:
+            cur.wait_stream(s)
+
+    reps = max(3, args.steps if args.steps < 1000 else 20)
+    for up, down, what in ((True, False, "h2d"), (False, True, "d2h"), (True, True, "both")):
+        for k in (1, 2, 4):
+            for _ in range(3):
+                run(k, up, down)
+            torch.cuda.synchronize()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cur)
+            for _ in range(reps):
+                run(k, up, down)
+            e.record(cur)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(e) / reps
+            nbytes = (n_in if up else 0) + (n_out if down else 0)
+            print(json.dumps({"link": what, "streams": k, "bytes": nbytes, "us": round(ms * 1e3, 1),
+                              "GB_s": round(nbytes / (ms / 1e3) / 1e9, 1), "reps": reps}),
+                  flush=True)
+
+
 # ------------------------------------------------------------------ main
 
 
@@ -1242,6 +1307,8 @@ def main(argv=None):
     ap.add_argument("--corun-budgets", default="2,4,8,16,0")
     ap.add_argument("--corun-reps", type=int, default=20)
     ap.add_argument("--offset-sweep", action="store_true")
+    ap.add_argument("--link", action="store_true",
+                    help="host-link copy bandwidth at the e2e leg's byte counts")
     ap.add_argument("--sweep-offsets-tokens",
                     default="1024,1536,2048,2560,3072,3584,4096,4864,5376,6144,7168,8192,9600")
     args = ap.parse_args(argv)
@@ -1256,6 +1323,9 @@ def main(argv=None):
         return
     if args.offset_sweep:
         offset_sweep(args)
+        return
+    if args.link:
+        link_probe(args)
         return
     if args.impl == "reference":
         # rank 0 alone times the oracle; other ranks exit without work
