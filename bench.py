@@ -1259,7 +1259,7 @@ def link_probe(args):
         for s in streams:
             cur.wait_stream(s)
 
-    reps = max(3, args.steps if args.steps < 1000 else 20)
+    reps = max(3, min(args.steps, 20))
     for up, down, what in ((True, False, "h2d"), (False, True, "d2h"), (True, True, "both")):
         for k in (1, 2, 4):
             for _ in range(3):
