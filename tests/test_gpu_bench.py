@@ -1,0 +1,57 @@
+"""The benchmark's own command on the GPU: a short default run prints one
+JSON line with the keys its readers take (the metric, the roofline block,
+the end-to-end leg with its host-link bound, the launch count and the clock
+record), and the host-link mode prints its nine cells. Needs a GPU."""
+
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args, timeout=600):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       capture_output=True, text=True, timeout=timeout)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_default_line_carries_the_contract_keys():
+    lines = _run("--steps", "5", "--warmup", "3", "--no-cpu-baseline", "--e2e-steps", "3",
+                 "--no-extras")
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["value"] > 0
+    assert d["config"]["workload"] == "llama70b_t1024_h8192_n8"
+    roof = d["roofline"]
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s"
+    assert roof["algorithmic_bytes"] == (8 + 3) * 1024 * 8192 * 2 + 8192 * 2
+    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
+    assert 0 < roof["frac_per_launch"] <= roof["frac"] * 1.05
+    e2e = d["e2e"]
+    assert e2e["h2d_bytes_per_step"] == 9 * 1024 * 8192 * 2 + 8192 * 2
+    assert e2e["d2h_bytes_per_step"] == 2 * 1024 * 8192 * 2
+    assert 0 < e2e["value"] < d["value"]
+    link = e2e["link_bound"]
+    # the copies alone cannot take longer than the copies plus the step, beyond noise
+    assert 0 < link["frac"] <= 1.1 and link["GB_s"] > 0
+    assert d["gpu_launches"] == 5
+    assert "sm_mhz" in d["clocks"] and "edges" in d["clocks"]
+    assert d["unfused"]["fused_speedup"] > 0
+
+
+def test_link_mode_prints_nine_cells():
+    lines = _run("--link", "--steps", "3")
+    assert [(l["link"], l["streams"]) for l in lines] == [
+        (w, k) for w in ("h2d", "d2h", "both") for k in (1, 2, 4)]
+    n_in, n_out = 9 * 1024 * 8192 * 2 + 8192 * 2, 2 * 1024 * 8192 * 2
+    for l in lines:
+        want = {"h2d": n_in, "d2h": n_out, "both": n_in + n_out}[l["link"]]
+        assert l["bytes"] == want and l["GB_s"] > 0
