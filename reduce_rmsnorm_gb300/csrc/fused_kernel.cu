@@ -31,9 +31,12 @@
 //     it can: two independent pipelines per CTA (each its own producer lanes,
 //     half of the ring and 8 consumer warps) for N <= 4, where the consumers'
 //     work per byte caps an SM; and the row ring (rowring_kernel), one bulk
-//     copy per source row, for N >= 9, where 4 KiB copies cap it. Each thread
-//     owns the same vectors and adds in the same order in every form, so the
-//     forms give bitwise the same rows; select_kernel picks one by speed.
+//     copy per source row, for N >= 9, where 4 KiB copies cap it. And with
+//     one row per CTA (decode-sized batches) the direct form (direct_kernel)
+//     loads each thread's vectors straight into registers, with no ring. Each
+//     thread owns the same vectors and adds in the same order in every form,
+//     so the forms give bitwise the same rows; select_kernel picks one by
+//     speed.
 //   * L2 policy per call: evict-first loads and a streaming output when no
 //     CTA owns more than one row and that row is over 144 KiB, for N <= 2 or
 //     N >= 9 with an output of at most an eighth of the L2, and for N <= 2
@@ -346,7 +349,7 @@ __device__ __forceinline__ void reduce_vector(uint32_t src, uint32_t cbytes, int
   }
 }
 
-// The end of a row, shared by both kernel forms: the sum of squares is
+// The end of a row, shared by every kernel form: the sum of squares is
 // reduced across the warp (xor shuffle) and then across the pipeline's 8
 // warps in warp order (through `wsum`, this row's 8 floats), r = rsqrt(mean +
 // eps), and Y = (z * r) * gamma is stored as bf16. With evict-first loads the
@@ -569,6 +572,71 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
     finish_row<KMAX, EXACT>(p, ss, z, g_reg, warp_ss[g][(row - ra) & 1], kConsumerBarrierId + g,
                             lane, wg, t, vpr, row);
   }
+}
+
+// Direct form, for launches of one row per CTA with whole-slot rows of
+// KMAX = 1, 2 or 4 slots (H = 2048, 4096, 8192) and a compile-time N <= 8.
+// Consumer thread t loads its own vectors t + 256 j of every source straight
+// into registers, so each byte crosses the SM's L1 once; the ring forms write
+// it into shared memory with a bulk copy and read it back. With one row per
+// CTA there is no later row for a ring to stage ahead, and the row is already
+// in L2 from the prefetch before the dependency wait. Thread t owns the same
+// vectors and adds the sources in the same rank order, then the residual, as
+// in fused_kernel, and the end of the row is finish_row, so rows are bitwise
+// those of the ring forms. No producer warp, no dynamic shared memory, no
+// mbarrier: the only wait is the CTA barrier inside finish_row.
+template <int KMAX, int NT>
+__global__ void __launch_bounds__(kConsumerThreads, 1)
+    direct_kernel(const __grid_constant__ Params p) {
+  __shared__ __align__(16) float warp_ss[kConsumerWarps];
+  static_assert(KMAX == 1 || KMAX == 2 || KMAX == 4, "one to four slots");
+  static_assert(NT >= 1 && NT <= 8, "compile-time N of 1..8");
+  constexpr int vpr = KMAX * kSlotVec;
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  const int wg = t >> 5;
+  const long long row = blockIdx.x;  // grid = rows
+  // L2 warm-up of the whole row before the dependency wait, as in
+  // fused_kernel: lane r of warp 0 asks for source r's row (r = N: the
+  // residual).
+  if (p.prefetch_bytes != 0 && wg == 0 && lane <= NT) {
+    const char* src =
+        reinterpret_cast<const char*>((lane < NT ? p.partials[lane] : p.residual) + row * vpr);
+    const uint32_t total = p.prefetch_bytes < static_cast<uint32_t>(vpr * 16)
+                               ? p.prefetch_bytes
+                               : static_cast<uint32_t>(vpr * 16);
+    for (uint32_t off = 0; off < total; off += kPrefetchPiece)
+      prefetch_l2(src + off, total - off < kPrefetchPiece ? total - off : kPrefetchPiece);
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (t == 0 && p.smid_out) p.smid_out[blockIdx.x] = static_cast<int>(sm_id());
+  uint4 g_reg[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) g_reg[j] = __ldg(p.gamma + j * kSlotVec + t);
+  // Every load of the row issues before the first add. The partials are
+  // loaded evict-first (their lines are not read again); the residual with
+  // the default policy, since this thread writes it back below.
+  uint4 q[KMAX][NT + 1];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+#pragma unroll
+    for (int r = 0; r < NT; ++r) q[j][r] = __ldcs(p.partials[r] + row * vpr + j * kSlotVec + t);
+    q[j][NT] = p.residual[row * vpr + j * kSlotVec + t];
+  }
+  float z[KMAX][8];
+  float ss = 0.0f;
+  uint4* res_row = p.residual + row * vpr;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    load8(q[j][0], z[j]);
+#pragma unroll
+    for (int r = 1; r <= NT; ++r) add8(q[j][r], z[j]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(z[j][i], z[j][i], ss);
+    res_row[j * kSlotVec + t] = pack8(z[j]);
+  }
+  finish_row<KMAX, true>(p, ss, z, g_reg, warp_ss, kConsumerBarrierId, lane, wg, t, vpr, row);
 }
 
 // Row-ring form: one bulk copy per (row, source), so a stage holds one
@@ -797,7 +865,13 @@ const KernelFn kChunkTwo[2][4] = {
     {fused_kernel<4, 2, 1, true, 2>, fused_kernel<4, 2, 2, true, 2>,
      fused_kernel<4, 2, 3, true, 2>, fused_kernel<4, 2, 4, true, 2>}};
 const KernelFn kRowTwo[2] = {rowring_kernel<4, 2, 0, true>, rowring_kernel<4, 2, 16, true>};
-constexpr int kNumKernels = 92 + 8 + 2;
+// Direct-form instances (one row per CTA): KMAX = 1, 2, 4 by N = 1..8.
+#define TW_DIRECT(K) {direct_kernel<K, 1>, direct_kernel<K, 2>, direct_kernel<K, 3>, \
+                      direct_kernel<K, 4>, direct_kernel<K, 5>, direct_kernel<K, 6>, \
+                      direct_kernel<K, 7>, direct_kernel<K, 8>}
+const KernelFn kDirect[3][8] = {TW_DIRECT(1), TW_DIRECT(2), TW_DIRECT(4)};
+#undef TW_DIRECT
+constexpr int kNumKernels = 92 + 8 + 2 + 24;
 
 // The kernel instance for a launch, and what its launch needs.
 struct Choice {
@@ -805,6 +879,7 @@ struct Choice {
   int index;    // attribute-cache slot
   int kmax;
   int rowring;  // 0: chunk ring (fused_kernel); 1: row ring (rowring_kernel)
+  int direct;   // 1: direct form (direct_kernel), no ring
   int groups;   // pipelines per CTA
   int vpt;      // chunk ring: slots per chunk
   int stages1;  // set by shape_for: two pipelines, pipeline 1's stages
@@ -863,9 +938,28 @@ int vpt_for(int n) { return n <= 8 ? 2 : 1; }
 //    an SM needs ~45 GB/s, the chunk ring is 2-4% faster. With one row per
 //    CTA one of the two pipelines idles and the chunk ring, with every
 //    source's chunks in flight, is 10-20% faster (T = 16-76, N = 9-16).
+//  * one row per CTA, N <= 8, H = 2048, 4096 or 8192: the direct form, with
+//    no staging in shared memory. Interleaved against the one-pipeline chunk
+//    ring at T = 32-152 (H = 4096, 8192; N = 2, 8): per launch up to 25%
+//    faster and never slower; back to back 8-17% faster at T = 128-152 and
+//    within 3% at T <= 64; from one CUDA graph 11-23% faster, except at
+//    H = 8192, N = 8, T <= 64 (-3% to +4%).
 //  * otherwise the chunk ring with one pipeline.
 Choice select_kernel(int vpr, int n, int64_t rows, int grid, int sms) {
   Choice c;
+  c.direct = 0;
+  if (rows <= grid && n <= 8 &&
+      (vpr == kSlotVec || vpr == 2 * kSlotVec || vpr == 4 * kSlotVec)) {
+    const int ki = vpr == kSlotVec ? 0 : (vpr == 2 * kSlotVec ? 1 : 2);
+    c.direct = 1;
+    c.kmax = vpr / kSlotVec;
+    c.rowring = 0;
+    c.groups = 1;
+    c.vpt = 1;  // unused
+    c.index = 102 + ki * 8 + (n - 1);
+    c.fn = kDirect[ki][n - 1];
+    return c;
+  }
   const int vpt = vpt_for(n);
   const int chunks = (vpr + kSlotVec * vpt - 1) / (kSlotVec * vpt);
   const int k = log2_pow2_at_least(chunks * vpt);  // KMAX = 2^k
@@ -935,6 +1029,19 @@ int shape_for(const DeviceInfo& d, int64_t rows, int64_t hidden, int n, int sm_b
               Choice* choice, LaunchShape* shape) {
   const int grid = grid_for(d, rows, sm_budget);
   const Choice c = select_kernel(static_cast<int>(hidden / 8), n, rows, grid, d.sms);
+  if (c.direct) {
+    Choice cc = c;
+    cc.stages1 = 0;
+    cc.split_num = 1;
+    cc.split_den = 2;
+    shape->grid = grid;
+    shape->threads = kConsumerThreads;
+    shape->smem_bytes = 0;
+    shape->stages = 0;
+    shape->kmax = c.kmax;
+    *choice = cc;
+    return TW_OK;
+  }
   // one stage: a source's row (row ring) or a chunk of every source (chunk ring)
   const int stage_bytes = c.rowring ? c.kmax * kSlotBytes : (n + 1) * kSlotBytes * c.vpt;
   int stages = (d.smem_optin - kStaticSmemReserve) / (c.groups * stage_bytes);
@@ -1048,7 +1155,7 @@ int launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_budget, int* sm
 
   const KernelFn fn = choice.fn;
   const int index = choice.index;
-  if (!d->attr_done[index].load(std::memory_order_acquire)) {
+  if (!choice.direct && !d->attr_done[index].load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!d->attr_done[index].load(std::memory_order_relaxed)) {
       const int max_dyn = d->smem_optin - kStaticSmemReserve;

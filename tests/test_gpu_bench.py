@@ -1,7 +1,8 @@
 """The benchmark's own command on the GPU: a short default run prints one
 JSON line with the keys its readers take (the metric, the roofline block,
 the end-to-end leg with its host-link bound, the launch count and the clock
-record), and the host-link mode prints its nine cells. Needs a GPU."""
+record), graph mode captures no graph inside the timed region, and the
+host-link mode prints its nine cells. Needs a GPU."""
 
 import json
 import os
@@ -55,3 +56,17 @@ def test_link_mode_prints_nine_cells():
     for l in lines:
         want = {"h2d": n_in, "d2h": n_out, "both": n_in + n_out}[l["link"]]
         assert l["bytes"] == want and l["GB_s"] > 0
+
+
+def test_graph_mode_captures_nothing_in_the_timed_region():
+    """Graph mode replays one graph per rotating input set; every graph is
+    captured during warm-up, so the timed steps are replays only."""
+    lines = _run("--workload", "pr1_t128_h4096_n2", "--mode", "graph", "--steps", "50",
+                 "--warmup", "3", "--no-cpu-baseline", "--e2e-steps", "3", "--no-extras",
+                 "--no-unfused")
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["config"]["graph_captures_in_region"] == 0
+    assert d["config"]["launch"].startswith("cuda graph")
+    assert d["value"] > 0
+

@@ -74,9 +74,11 @@ def _one_case_per_instance():
     is the smallest power of two >= the row's chunks * VPT; a row is EXACT
     when H / 8 == KMAX * 256. For each KMAX an exact H and a ragged H of the
     same KMAX are paired with every N of the compile-time instances and with
-    N that take the runtime-N instance."""
+    N that take the runtime-N instance. At one row per CTA, H = 2048, 4096
+    and 8192 with N <= 8 take the direct form (KMAX = H / 2048)."""
     cases = []
-    for exact, ragged in ((4096, 2056), (8192, 6152), (16384, 12296), (32768, 24584)):
+    for exact, ragged in ((2048, 1032), (4096, 2056), (8192, 6152), (16384, 12296),
+                          (32768, 24584)):
         for n in range(1, 9):
             cases += [(exact, n), (ragged, n)]
     for exact, ragged in ((2048, 1032), (4096, 3080), (8192, 6152), (16384, 12296),
@@ -89,7 +91,8 @@ def _one_case_per_instance():
 @pytest.mark.parametrize("T,budget", [(3, 0), (40, 3)])
 @pytest.mark.parametrize("H,N", _one_case_per_instance())
 def test_parity_every_kernel_instance(H, N, T, budget):
-    """T=3: one row per CTA (the L2 prefetch is issued when the row fits in
+    """T=3: one row per CTA (the direct form for whole-slot H <= 8192 and
+    N <= 8, a ring otherwise; the L2 prefetch is issued when the row fits in
     144 KiB); T=40 on 3 SMs: 13-14 rows per CTA, so the ring wraps across
     rows, the prefetch is issued, and KMAX = 4 shapes take the two-pipeline
     forms."""
@@ -560,11 +563,12 @@ def _random_two_pipeline_shapes(count, seed):
 def test_parity_random_two_pipeline_shapes(T, H, N, budget):
     """Seeded random shapes in the two-pipeline forms, every row checked
     against the oracle, and bitwise equal to the whole-GPU launch of the same
-    rows, which takes the one-pipeline chunk ring (its CTAs own under 4 rows,
-    or one row each)."""
+    rows. There every CTA owns one row: the direct form at H = 8192 with
+    N <= 8, the one-pipeline chunk ring otherwise."""
     shape = tw.tw_launch_shape(T, H, N, budget)
     assert shape["threads"] == 544, (T, H, N, budget, shape)
-    assert tw.tw_launch_shape(T, H, N, 0)["threads"] == 288
+    direct = H == 8192 and N <= 8
+    assert tw.tw_launch_shape(T, H, N, 0)["threads"] == (256 if direct else 288)
     p, r, g = synth.make_inputs(T, H, N, 0.03, seed=T + H + N + budget)
     R, out = run(p, r, g, sm_budget=budget)
     check_rows(p, r, g, EPS, R, out)
@@ -590,6 +594,48 @@ def test_one_row_per_cta_takes_the_chunk_ring(T, N):
     R4, out4 = run(p, r, g, sm_budget=4)
     assert_same(R, R4)
     assert_same(out, out4)
+
+
+@pytest.mark.parametrize("H", [2048, 4096, 8192])
+@pytest.mark.parametrize("N", [1, 3, 5, 8])
+def test_direct_form_against_the_ring_and_the_oracle(H, N):
+    """One row per CTA with H = 2048, 4096 or 8192 and N <= 8 takes the
+    direct form (no producer warp, no shared-memory ring). T = 152 on the
+    whole GPU against the same rows under an 8-SM budget (19 rows per CTA:
+    a ring form) bit for bit, and every row against the oracle."""
+    T = 152
+    full = tw.tw_launch_shape(T, H, N, 0)
+    assert (full["threads"], full["smem_bytes"], full["stages"]) == (256, 0, 0), full
+    assert tw.tw_launch_shape(T, H, N, 8)["smem_bytes"] > 0
+    p, r, g = synth.make_inputs(T, H, N, 0.02, outlier_frac=0.01, seed=H + 11 * N)
+    R, out = run(p, r, g)
+    check_rows(p, r, g, EPS, R, out)
+    R8, out8 = run(p, r, g, sm_budget=8)
+    assert_same(R, R8)
+    assert_same(out, out8)
+
+
+@pytest.mark.parametrize("T", [1, 7, 100])
+def test_direct_form_output_over_a_partial_and_smid(T):
+    """The direct form with Y written over partial 5, against Y into its own
+    buffer; and its %smid record names a valid SM for every CTA."""
+    H, N = 8192, 8
+    p, r, g = synth.make_inputs(T, H, N, 0.02, seed=300 + T)
+    ref = run(p, r, g)
+    P, R, G = to_gpu(p, r, g)
+    out = P[5]
+    tw.tw_fused_reduce_residual_rmsnorm(P, R, G, EPS, out)
+    torch.cuda.synchronize()
+    assert_same(ref[0], R)
+    assert_same(ref[1], out)
+    P, R, G = to_gpu(p, r, g)
+    out = torch.empty_like(R)
+    smid = torch.full((T,), -1, dtype=torch.int32, device="cuda")
+    tw.tw_fused_debug_smid(P, R, G, EPS, out, smid)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert int(smid.min()) >= 0 and int(smid.max()) < sms
+    assert_same(ref[1], out)
 
 
 @pytest.mark.parametrize("which,budget,split,N", [(0, 0, False, 8), (7, 0, False, 8),
