@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
 }
 
 // Direct form, for launches of one row per CTA with whole-slot rows of
-// KMAX = 1, 2 or 4 slots (H = 2048, 4096, 8192) and a compile-time N <= 8.
+// KMAX = 1, 2, 4 or 8 slots (H = 2048 to 16384) and a compile-time N <= 8.
 // Consumer thread t loads its own vectors t + 256 j of every source straight
 // into registers, so each byte crosses the SM's L1 once; the ring forms write
 // it into shared memory with a bulk copy and read it back. With one row per
@@ -589,7 +589,7 @@ template <int KMAX, int NT>
 __global__ void __launch_bounds__(kConsumerThreads, 1)
     direct_kernel(const __grid_constant__ Params p) {
   __shared__ __align__(16) float warp_ss[kConsumerWarps];
-  static_assert(KMAX == 1 || KMAX == 2 || KMAX == 4, "one to four slots");
+  static_assert(KMAX == 1 || KMAX == 2 || KMAX == 4 || KMAX == 8, "one to eight slots");
   static_assert(NT >= 1 && NT <= 8, "compile-time N of 1..8");
   constexpr int vpr = KMAX * kSlotVec;
   const int t = threadIdx.x;
@@ -865,13 +865,13 @@ const KernelFn kChunkTwo[2][4] = {
     {fused_kernel<4, 2, 1, true, 2>, fused_kernel<4, 2, 2, true, 2>,
      fused_kernel<4, 2, 3, true, 2>, fused_kernel<4, 2, 4, true, 2>}};
 const KernelFn kRowTwo[2] = {rowring_kernel<4, 2, 0, true>, rowring_kernel<4, 2, 16, true>};
-// Direct-form instances (one row per CTA): KMAX = 1, 2, 4 by N = 1..8.
+// Direct-form instances (one row per CTA): KMAX = 1, 2, 4, 8 by N = 1..8.
 #define TW_DIRECT(K) {direct_kernel<K, 1>, direct_kernel<K, 2>, direct_kernel<K, 3>, \
                       direct_kernel<K, 4>, direct_kernel<K, 5>, direct_kernel<K, 6>, \
                       direct_kernel<K, 7>, direct_kernel<K, 8>}
-const KernelFn kDirect[3][8] = {TW_DIRECT(1), TW_DIRECT(2), TW_DIRECT(4)};
+const KernelFn kDirect[4][8] = {TW_DIRECT(1), TW_DIRECT(2), TW_DIRECT(4), TW_DIRECT(8)};
 #undef TW_DIRECT
-constexpr int kNumKernels = 92 + 8 + 2 + 24;
+constexpr int kNumKernels = 92 + 8 + 2 + 32;
 
 // The kernel instance for a launch, and what its launch needs.
 struct Choice {
@@ -938,19 +938,21 @@ int vpt_for(int n) { return n <= 8 ? 2 : 1; }
 //    an SM needs ~45 GB/s, the chunk ring is 2-4% faster. With one row per
 //    CTA one of the two pipelines idles and the chunk ring, with every
 //    source's chunks in flight, is 10-20% faster (T = 16-76, N = 9-16).
-//  * one row per CTA, N <= 8, H = 2048, 4096 or 8192: the direct form, with
-//    no staging in shared memory. Interleaved against the one-pipeline chunk
-//    ring at T = 32-152 (H = 4096, 8192; N = 2, 8): per launch up to 25%
-//    faster and never slower; back to back 8-17% faster at T = 128-152 and
-//    within 3% at T <= 64; from one CUDA graph 11-23% faster, except at
-//    H = 8192, N = 8, T <= 64 (-3% to +4%).
+//  * one row per CTA, N <= 8, H = 2048, 4096, 8192 or 16384: the direct
+//    form, with no staging in shared memory. Interleaved against the
+//    one-pipeline chunk ring at T = 32-152 (H = 4096, 8192; N = 2, 8): per
+//    launch up to 25% faster and never slower; back to back 8-17% faster at
+//    T = 128-152 and within 3% at T <= 64; from one CUDA graph 11-23% faster,
+//    except at H = 8192, N = 8, T <= 64 (-3% to +4%). At H = 16384 (N = 2, 4,
+//    8) never slower per launch; back to back 9-22% faster at N = 2, 3-7% at
+//    N = 8, unchanged at N = 4.
 //  * otherwise the chunk ring with one pipeline.
 Choice select_kernel(int vpr, int n, int64_t rows, int grid, int sms) {
   Choice c;
   c.direct = 0;
   if (rows <= grid && n <= 8 &&
-      (vpr == kSlotVec || vpr == 2 * kSlotVec || vpr == 4 * kSlotVec)) {
-    const int ki = vpr == kSlotVec ? 0 : (vpr == 2 * kSlotVec ? 1 : 2);
+      (vpr == kSlotVec || vpr == 2 * kSlotVec || vpr == 4 * kSlotVec || vpr == 8 * kSlotVec)) {
+    const int ki = vpr == kSlotVec ? 0 : (vpr == 2 * kSlotVec ? 1 : (vpr == 4 * kSlotVec ? 2 : 3));
     c.direct = 1;
     c.kmax = vpr / kSlotVec;
     c.rowring = 0;

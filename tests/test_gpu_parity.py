@@ -74,8 +74,8 @@ def _one_case_per_instance():
     is the smallest power of two >= the row's chunks * VPT; a row is EXACT
     when H / 8 == KMAX * 256. For each KMAX an exact H and a ragged H of the
     same KMAX are paired with every N of the compile-time instances and with
-    N that take the runtime-N instance. At one row per CTA, H = 2048, 4096
-    and 8192 with N <= 8 take the direct form (KMAX = H / 2048)."""
+    N that take the runtime-N instance. At one row per CTA, H = 2048, 4096,
+    8192 and 16384 with N <= 8 take the direct form (KMAX = H / 2048)."""
     cases = []
     for exact, ragged in ((2048, 1032), (4096, 2056), (8192, 6152), (16384, 12296),
                           (32768, 24584)):
@@ -91,7 +91,7 @@ def _one_case_per_instance():
 @pytest.mark.parametrize("T,budget", [(3, 0), (40, 3)])
 @pytest.mark.parametrize("H,N", _one_case_per_instance())
 def test_parity_every_kernel_instance(H, N, T, budget):
-    """T=3: one row per CTA (the direct form for whole-slot H <= 8192 and
+    """T=3: one row per CTA (the direct form for whole-slot H <= 16384 and
     N <= 8, a ring otherwise; the L2 prefetch is issued when the row fits in
     144 KiB); T=40 on 3 SMs: 13-14 rows per CTA, so the ring wraps across
     rows, the prefetch is issued, and KMAX = 4 shapes take the two-pipeline
@@ -596,10 +596,10 @@ def test_one_row_per_cta_takes_the_chunk_ring(T, N):
     assert_same(out, out4)
 
 
-@pytest.mark.parametrize("H", [2048, 4096, 8192])
+@pytest.mark.parametrize("H", [2048, 4096, 8192, 16384])
 @pytest.mark.parametrize("N", [1, 3, 5, 8])
 def test_direct_form_against_the_ring_and_the_oracle(H, N):
-    """One row per CTA with H = 2048, 4096 or 8192 and N <= 8 takes the
+    """One row per CTA with H = 2048, 4096, 8192 or 16384 and N <= 8 takes the
     direct form (no producer warp, no shared-memory ring). T = 152 on the
     whole GPU against the same rows under an 8-SM budget (19 rows per CTA:
     a ring form) bit for bit, and every row against the oracle."""
