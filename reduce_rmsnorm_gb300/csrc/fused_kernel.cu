@@ -574,8 +574,10 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
   }
 }
 
-// Direct form, for launches of one row per CTA with whole-slot rows of
-// KMAX = 1, 2, 4 or 8 slots (H = 2048 to 16384) and a compile-time N <= 8.
+// Direct form, for launches of one row per CTA of at most 8 slots (H <= 16384)
+// and a compile-time N <= 8. KMAX is the slot count rounded up to a power of
+// two; EXACT rows fill it (H = 2048, 4096, 8192, 16384), other rows check
+// each vector against the row's end, as fused_kernel does.
 // Consumer thread t loads its own vectors t + 256 j of every source straight
 // into registers, so each byte crosses the SM's L1 once; the ring forms write
 // it into shared memory with a bulk copy and read it back. With one row per
@@ -585,13 +587,13 @@ __global__ void __launch_bounds__(G * kConsumerThreads + 32, 1)
 // in fused_kernel, and the end of the row is finish_row, so rows are bitwise
 // those of the ring forms. No producer warp, no dynamic shared memory, no
 // mbarrier: the only wait is the CTA barrier inside finish_row.
-template <int KMAX, int NT>
+template <int KMAX, int NT, bool EXACT>
 __global__ void __launch_bounds__(kConsumerThreads, 1)
     direct_kernel(const __grid_constant__ Params p) {
   __shared__ __align__(16) float warp_ss[kConsumerWarps];
   static_assert(KMAX == 1 || KMAX == 2 || KMAX == 4 || KMAX == 8, "one to eight slots");
   static_assert(NT >= 1 && NT <= 8, "compile-time N of 1..8");
-  constexpr int vpr = KMAX * kSlotVec;
+  const int vpr = EXACT ? KMAX * kSlotVec : p.vec_per_row;
   const int t = threadIdx.x;
   const int lane = t & 31;
   const int wg = t >> 5;
@@ -613,30 +615,39 @@ __global__ void __launch_bounds__(kConsumerThreads, 1)
   if (t == 0 && p.smid_out) p.smid_out[blockIdx.x] = static_cast<int>(sm_id());
   uint4 g_reg[KMAX];
 #pragma unroll
-  for (int j = 0; j < KMAX; ++j) g_reg[j] = __ldg(p.gamma + j * kSlotVec + t);
+  for (int j = 0; j < KMAX; ++j) {
+    const int v = j * kSlotVec + t;
+    g_reg[j] = (EXACT || v < vpr) ? __ldg(p.gamma + v) : make_uint4(0, 0, 0, 0);
+  }
   // Every load of the row issues before the first add. The partials are
   // loaded evict-first (their lines are not read again); the residual with
   // the default policy, since this thread writes it back below.
   uint4 q[KMAX][NT + 1];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
+    const int v = j * kSlotVec + t;
+    if (EXACT || v < vpr) {
 #pragma unroll
-    for (int r = 0; r < NT; ++r) q[j][r] = __ldcs(p.partials[r] + row * vpr + j * kSlotVec + t);
-    q[j][NT] = p.residual[row * vpr + j * kSlotVec + t];
+      for (int r = 0; r < NT; ++r) q[j][r] = __ldcs(p.partials[r] + row * vpr + v);
+      q[j][NT] = p.residual[row * vpr + v];
+    }
   }
   float z[KMAX][8];
   float ss = 0.0f;
   uint4* res_row = p.residual + row * vpr;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) {
-    load8(q[j][0], z[j]);
+    const int v = j * kSlotVec + t;
+    if (EXACT || v < vpr) {
+      load8(q[j][0], z[j]);
 #pragma unroll
-    for (int r = 1; r <= NT; ++r) add8(q[j][r], z[j]);
+      for (int r = 1; r <= NT; ++r) add8(q[j][r], z[j]);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(z[j][i], z[j][i], ss);
-    res_row[j * kSlotVec + t] = pack8(z[j]);
+      for (int i = 0; i < 8; ++i) ss = fmaf(z[j][i], z[j][i], ss);
+      res_row[v] = pack8(z[j]);
+    }
   }
-  finish_row<KMAX, true>(p, ss, z, g_reg, warp_ss, kConsumerBarrierId, lane, wg, t, vpr, row);
+  finish_row<KMAX, EXACT>(p, ss, z, g_reg, warp_ss, kConsumerBarrierId, lane, wg, t, vpr, row);
 }
 
 // Row-ring form: one bulk copy per (row, source), so a stage holds one
@@ -865,13 +876,20 @@ const KernelFn kChunkTwo[2][4] = {
     {fused_kernel<4, 2, 1, true, 2>, fused_kernel<4, 2, 2, true, 2>,
      fused_kernel<4, 2, 3, true, 2>, fused_kernel<4, 2, 4, true, 2>}};
 const KernelFn kRowTwo[2] = {rowring_kernel<4, 2, 0, true>, rowring_kernel<4, 2, 16, true>};
-// Direct-form instances (one row per CTA): KMAX = 1, 2, 4, 8 by N = 1..8.
-#define TW_DIRECT(K) {direct_kernel<K, 1>, direct_kernel<K, 2>, direct_kernel<K, 3>, \
-                      direct_kernel<K, 4>, direct_kernel<K, 5>, direct_kernel<K, 6>, \
-                      direct_kernel<K, 7>, direct_kernel<K, 8>}
-const KernelFn kDirect[4][8] = {TW_DIRECT(1), TW_DIRECT(2), TW_DIRECT(4), TW_DIRECT(8)};
+// Direct-form instances (one row per CTA): ragged and EXACT, KMAX = 1, 2, 4,
+// 8, N = 1..8. The ragged KMAX = 8 instances for N = 6..8 spilled (96-440
+// bytes of stack at the 255-register limit) and are not built: those shapes
+// keep the chunk ring.
+#define TW_DIRECT(K, E) {direct_kernel<K, 1, E>, direct_kernel<K, 2, E>, direct_kernel<K, 3, E>, \
+                         direct_kernel<K, 4, E>, direct_kernel<K, 5, E>, direct_kernel<K, 6, E>, \
+                         direct_kernel<K, 7, E>, direct_kernel<K, 8, E>}
+const KernelFn kDirect[2][4][8] = {
+    {TW_DIRECT(1, false), TW_DIRECT(2, false), TW_DIRECT(4, false),
+     {direct_kernel<8, 1, false>, direct_kernel<8, 2, false>, direct_kernel<8, 3, false>,
+      direct_kernel<8, 4, false>, direct_kernel<8, 5, false>, nullptr, nullptr, nullptr}},
+    {TW_DIRECT(1, true), TW_DIRECT(2, true), TW_DIRECT(4, true), TW_DIRECT(8, true)}};
 #undef TW_DIRECT
-constexpr int kNumKernels = 92 + 8 + 2 + 32;
+constexpr int kNumKernels = 92 + 8 + 2 + 64;
 
 // The kernel instance for a launch, and what its launch needs.
 struct Choice {
@@ -938,28 +956,31 @@ int vpt_for(int n) { return n <= 8 ? 2 : 1; }
 //    an SM needs ~45 GB/s, the chunk ring is 2-4% faster. With one row per
 //    CTA one of the two pipelines idles and the chunk ring, with every
 //    source's chunks in flight, is 10-20% faster (T = 16-76, N = 9-16).
-//  * one row per CTA, N <= 8, H = 2048, 4096, 8192 or 16384: the direct
-//    form, with no staging in shared memory. Interleaved against the
+//  * one row per CTA, N <= 8, H <= 16384 (but not N >= 6 with H over 8192
+//    and short of 16384): the direct form, with no staging in shared memory. Interleaved against the
 //    one-pipeline chunk ring at T = 32-152 (H = 4096, 8192; N = 2, 8): per
 //    launch up to 25% faster and never slower; back to back 8-17% faster at
 //    T = 128-152 and within 3% at T <= 64; from one CUDA graph 11-23% faster,
 //    except at H = 8192, N = 8, T <= 64 (-3% to +4%). At H = 16384 (N = 2, 4,
 //    8) never slower per launch; back to back 9-22% faster at N = 2, 3-7% at
-//    N = 8, unchanged at N = 4.
+//    N = 8, unchanged at N = 4. Ragged rows (H = 1024, 3072, 5120, 6144,
+//    7168, 12288; N = 2, 8; T = 32-152): never slower per launch, from one
+//    CUDA graph 5-30% faster, back to back mostly 5-17% faster.
 //  * otherwise the chunk ring with one pipeline.
 Choice select_kernel(int vpr, int n, int64_t rows, int grid, int sms) {
   Choice c;
   c.direct = 0;
-  if (rows <= grid && n <= 8 &&
-      (vpr == kSlotVec || vpr == 2 * kSlotVec || vpr == 4 * kSlotVec || vpr == 8 * kSlotVec)) {
-    const int ki = vpr == kSlotVec ? 0 : (vpr == 2 * kSlotVec ? 1 : (vpr == 4 * kSlotVec ? 2 : 3));
+  const int dk = log2_pow2_at_least((vpr + kSlotVec - 1) / kSlotVec);  // direct KMAX = 2^dk
+  const int dexact = vpr == (1 << dk) * kSlotVec ? 1 : 0;
+  if (rows <= grid && n <= 8 && dk <= 3 && kDirect[dexact][dk][n - 1] != nullptr) {
+    const int ki = dk, exact = dexact;
     c.direct = 1;
-    c.kmax = vpr / kSlotVec;
+    c.kmax = 1 << ki;
     c.rowring = 0;
     c.groups = 1;
     c.vpt = 1;  // unused
-    c.index = 102 + ki * 8 + (n - 1);
-    c.fn = kDirect[ki][n - 1];
+    c.index = 102 + exact * 32 + ki * 8 + (n - 1);
+    c.fn = kDirect[exact][ki][n - 1];
     return c;
   }
   const int vpt = vpt_for(n);

@@ -74,8 +74,10 @@ def _one_case_per_instance():
     is the smallest power of two >= the row's chunks * VPT; a row is EXACT
     when H / 8 == KMAX * 256. For each KMAX an exact H and a ragged H of the
     same KMAX are paired with every N of the compile-time instances and with
-    N that take the runtime-N instance. At one row per CTA, H = 2048, 4096,
-    8192 and 16384 with N <= 8 take the direct form (KMAX = H / 2048)."""
+    N that take the runtime-N instance. At one row per CTA, N <= 8 with
+    H <= 16384 takes the direct form (its own KMAX: the row's 256-vector
+    slots rounded up to a power of two), but for ragged rows over 8192 with
+    N >= 6."""
     cases = []
     for exact, ragged in ((2048, 1032), (4096, 2056), (8192, 6152), (16384, 12296),
                           (32768, 24584)):
@@ -91,8 +93,8 @@ def _one_case_per_instance():
 @pytest.mark.parametrize("T,budget", [(3, 0), (40, 3)])
 @pytest.mark.parametrize("H,N", _one_case_per_instance())
 def test_parity_every_kernel_instance(H, N, T, budget):
-    """T=3: one row per CTA (the direct form for whole-slot H <= 16384 and
-    N <= 8, a ring otherwise; the L2 prefetch is issued when the row fits in
+    """T=3: one row per CTA (the direct form for H <= 16384 and N <= 8
+    except ragged rows over 8192 with N >= 6, a ring otherwise; the L2 prefetch is issued when the row fits in
     144 KiB); T=40 on 3 SMs: 13-14 rows per CTA, so the ring wraps across
     rows, the prefetch is issued, and KMAX = 4 shapes take the two-pipeline
     forms."""
@@ -563,12 +565,11 @@ def _random_two_pipeline_shapes(count, seed):
 def test_parity_random_two_pipeline_shapes(T, H, N, budget):
     """Seeded random shapes in the two-pipeline forms, every row checked
     against the oracle, and bitwise equal to the whole-GPU launch of the same
-    rows. There every CTA owns one row: the direct form at H = 8192 with
-    N <= 8, the one-pipeline chunk ring otherwise."""
+    rows. There every CTA owns one row: the direct form for N <= 8, the
+    one-pipeline chunk ring otherwise."""
     shape = tw.tw_launch_shape(T, H, N, budget)
     assert shape["threads"] == 544, (T, H, N, budget, shape)
-    direct = H == 8192 and N <= 8
-    assert tw.tw_launch_shape(T, H, N, 0)["threads"] == (256 if direct else 288)
+    assert tw.tw_launch_shape(T, H, N, 0)["threads"] == (256 if _takes_direct(H, N) else 288)
     p, r, g = synth.make_inputs(T, H, N, 0.03, seed=T + H + N + budget)
     R, out = run(p, r, g, sm_budget=budget)
     check_rows(p, r, g, EPS, R, out)
@@ -596,16 +597,31 @@ def test_one_row_per_cta_takes_the_chunk_ring(T, N):
     assert_same(out, out4)
 
 
-@pytest.mark.parametrize("H", [2048, 4096, 8192, 16384])
+def _takes_direct(H, N):
+    """The direct form's domain at one row per CTA: N <= 8 and at most 8
+    slots of 256 vectors, except ragged rows of 5-8 slots with N >= 6 (those
+    instances spilled and are not built)."""
+    slots = -(-(H // 8) // 256)
+    kmax = 1 << (slots - 1).bit_length()
+    exact = H // 8 == kmax * 256
+    return N <= 8 and kmax <= 8 and not (kmax == 8 and not exact and N >= 6)
+
+
+@pytest.mark.parametrize("H", [2048, 4096, 8192, 16384, 1032, 5120, 12296])
 @pytest.mark.parametrize("N", [1, 3, 5, 8])
 def test_direct_form_against_the_ring_and_the_oracle(H, N):
-    """One row per CTA with H = 2048, 4096, 8192 or 16384 and N <= 8 takes the
-    direct form (no producer warp, no shared-memory ring). T = 152 on the
-    whole GPU against the same rows under an 8-SM budget (19 rows per CTA:
-    a ring form) bit for bit, and every row against the oracle."""
+    """One row per CTA with N <= 8 and H <= 16384 takes the direct form (no
+    producer warp, no shared-memory ring), whole-slot rows (H = 2048, 4096,
+    8192, 16384) and ragged ones alike, except ragged rows over 8192 with
+    N >= 6. T = 152 on the whole GPU against the same rows under an 8-SM
+    budget (19 rows per CTA: a ring form) bit for bit, and every row against
+    the oracle."""
     T = 152
     full = tw.tw_launch_shape(T, H, N, 0)
-    assert (full["threads"], full["smem_bytes"], full["stages"]) == (256, 0, 0), full
+    if _takes_direct(H, N):
+        assert (full["threads"], full["smem_bytes"], full["stages"]) == (256, 0, 0), full
+    else:
+        assert full["threads"] == 288 and full["smem_bytes"] > 0, full
     assert tw.tw_launch_shape(T, H, N, 8)["smem_bytes"] > 0
     p, r, g = synth.make_inputs(T, H, N, 0.02, outlier_frac=0.01, seed=H + 11 * N)
     R, out = run(p, r, g)
