@@ -105,9 +105,10 @@ typedef enum {
  *              other SMs ([W] "What it buys": 2 to 8 SMs). A CTA that owns
  *              more than one row requests enough shared memory that no second
  *              CTA of this kernel fits on its SM; with one row per CTA (T <= k
- *              or T <= the SM count) it requests only that row's staging, so
- *              small rows may share an SM with the next launch's CTAs. k above
- *              the SM count is clamped. Negative is invalid.
+ *              or T <= the SM count) it stages at most that row (for N <= 8
+ *              and H <= 16384 it loads the row into registers, with no
+ *              staging), so such CTAs may share an SM with the next launch's
+ *              CTAs. k above the SM count is clamped. Negative is invalid.
  *
  * Errors: TW_ERR_INVALID_ARG (N, T, H <= 0, eps, sm_budget, a null pointer,
  * residual/out overlapping each other or any input other than out ==
@@ -281,8 +282,10 @@ TW_API const char* tw_strerror(int status);
 /*
  * tw_launch_shape -- the launch the fused call would make on the current
  * device: grid (CTAs, = SMs used), threads per CTA, dynamic shared memory
- * bytes and pipeline stages. Any output pointer may be NULL. Queries device
- * attributes (TW_ERR_CUDA without a GPU). Validation as for the fused call.
+ * bytes and pipeline stages (0 stages and 0 bytes for a launch that loads
+ * its one row per CTA straight into registers). Any output pointer may be
+ * NULL. Queries device attributes (TW_ERR_CUDA without a GPU). Validation as
+ * for the fused call.
  */
 TW_API int tw_launch_shape(int64_t T, int64_t H, int N, int sm_budget, int* grid, int* threads,
                     int* smem_bytes, int* stages);
