@@ -912,6 +912,7 @@ struct DeviceInfo {
   int sms;
   int smem_optin;
   int l2_bytes;
+  int regs_per_sm;
   std::atomic<bool> attr_done[kNumKernels];
 };
 
@@ -1032,6 +1033,9 @@ int device_info(DeviceInfo** out) {
         return TW_ERR_CUDA;
       if (cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
         return TW_ERR_CUDA;
+      if (cudaDeviceGetAttribute(&d.regs_per_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) !=
+          cudaSuccess)
+        return TW_ERR_CUDA;
       d.ready.store(true, std::memory_order_release);
     }
   }
@@ -1047,10 +1051,43 @@ int grid_for(const DeviceInfo& d, int64_t rows, int sm_budget) {
   return grid;
 }
 
+// Registers per thread of each instance, queried once (0: not yet known).
+// They are a property of the compiled code, the same on every device.
+std::atomic<int> g_kernel_regs[kNumKernels];
+
+// Whether two CTAs of a direct-form instance fit in one SM's registers
+// (allocated per warp in units of 8 registers a thread).
+bool two_direct_ctas_fit(const DeviceInfo& d, const Choice& c) {
+  int r = g_kernel_regs[c.index].load(std::memory_order_relaxed);
+  if (r == 0) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, c.fn) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    r = a.numRegs;
+    g_kernel_regs[c.index].store(r, std::memory_order_relaxed);
+  }
+  const int per_cta = (r + 7) / 8 * 8 * kConsumerThreads;
+  return 2 * per_cta <= d.regs_per_sm;
+}
+
 // The launch of `rows` rows: the instance (*choice) and its shape.
 int shape_for(const DeviceInfo& d, int64_t rows, int64_t hidden, int n, int sm_budget,
               Choice* choice, LaunchShape* shape) {
-  const int grid = grid_for(d, rows, sm_budget);
+  int grid = grid_for(d, rows, sm_budget);
+  if (sm_budget == 0 && rows > grid && rows <= 2 * static_cast<int64_t>(d.sms)) {
+    // On the whole GPU with up to two rows per SM: one direct-form CTA per
+    // row, where two such CTAs fit on an SM, instead of a ring CTA per SM
+    // that owns two rows. Interleaved at T = 160-304 against the ring: per
+    // launch never slower, from one CUDA graph 1-30% faster and back to back
+    // 1-22% faster at H = 4096 (N = 2, 4, 8) and H = 8192 (N = 2, 4); at
+    // H = 8192, N = 8 (144 registers: one CTA per SM, so two waves) 6-17%
+    // slower back to back, which the register check excludes.
+    const Choice w = select_kernel(static_cast<int>(hidden / 8), n, rows, static_cast<int>(rows),
+                                   d.sms);
+    if (w.direct && two_direct_ctas_fit(d, w)) grid = static_cast<int>(rows);
+  }
   const Choice c = select_kernel(static_cast<int>(hidden / 8), n, rows, grid, d.sms);
   if (c.direct) {
     Choice cc = c;

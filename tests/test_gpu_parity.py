@@ -631,6 +631,31 @@ def test_direct_form_against_the_ring_and_the_oracle(H, N):
     assert_same(out, out8)
 
 
+@pytest.mark.parametrize("T,H,N", [(160, 4096, 8), (256, 4096, 2), (304, 8192, 4),
+                                   (200, 6144, 2), (300, 16384, 2), (256, 8192, 8),
+                                   (305, 4096, 2)])
+def test_one_cta_per_row_up_to_two_rows_per_sm(T, H, N):
+    """On the whole GPU with more rows than SMs but at most two per SM, one
+    direct-form CTA per row where two such CTAs fit in an SM's registers, a
+    ring CTA per SM otherwise (H = 8192, N = 8: 144 registers a thread; and
+    beyond two rows per SM). Every row against the oracle, and bit for bit
+    against the same rows under an 8-SM budget (a ring form)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shape = tw.tw_launch_shape(T, H, N, 0)
+    direct = shape["threads"] == 256
+    assert shape["grid"] == (T if direct else min(T, sms)), shape
+    if (T, H, N) == (160, 4096, 8):
+        assert direct
+    if (T, H, N) in ((256, 8192, 8), (305, 4096, 2)):
+        assert not direct
+    p, r, g = synth.make_inputs(T, H, N, 0.02, seed=T + H + N)
+    R, out = run(p, r, g)
+    check_rows(p, r, g, EPS, R, out)
+    R8, out8 = run(p, r, g, sm_budget=8)
+    assert_same(R, R8)
+    assert_same(out, out8)
+
+
 @pytest.mark.parametrize("T", [1, 7, 100])
 def test_direct_form_output_over_a_partial_and_smid(T):
     """The direct form with Y written over partial 5, against Y into its own
