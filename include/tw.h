@@ -99,9 +99,10 @@ typedef enum {
  *              one partial (out == partials[r]) to write Y over that rank's
  *              partial; no other overlap with an input is allowed.
  *   stream     the stream to launch on.
- *   sm_budget  0: use the whole GPU (one CTA per SM; with more rows than SMs
- *              but at most two per SM, one CTA per row where two such CTAs
- *              fit on an SM). k > 0: launch at most k
+ *   sm_budget  0: use the whole GPU (one CTA per SM; with more rows than SMs,
+ *              one CTA per row while all of them fit on the GPU at once, which
+ *              the register-loading form allows for small rows and small N).
+ *              k > 0: launch at most k
  *              CTAs, each owning a contiguous range of about T / k rows, so
  *              the step occupies at most k SMs and co-runs with work on the
  *              other SMs ([W] "What it buys": 2 to 8 SMs). A CTA that owns

@@ -1056,7 +1056,8 @@ int grid_for(const DeviceInfo& d, int64_t rows, int sm_budget) {
 std::atomic<int> g_kernel_regs[kNumKernels];
 
 // Whether two CTAs of a direct-form instance fit in one SM's registers
-// (allocated per warp in units of 8 registers a thread).
+// (allocated per warp in units of 8 registers a thread), which also caches
+// the instance's register count.
 bool two_direct_ctas_fit(const DeviceInfo& d, const Choice& c) {
   int r = g_kernel_regs[c.index].load(std::memory_order_relaxed);
   if (r == 0) {
@@ -1071,22 +1072,34 @@ bool two_direct_ctas_fit(const DeviceInfo& d, const Choice& c) {
   const int per_cta = (r + 7) / 8 * 8 * kConsumerThreads;
   return 2 * per_cta <= d.regs_per_sm;
 }
+// How many CTAs of a direct-form instance an SM holds at once: by registers,
+// and at most 8 (2048 threads of 256).
+int direct_ctas_per_sm(const DeviceInfo& d, const Choice& c) {
+  if (!two_direct_ctas_fit(d, c)) return 1;
+  const int r = g_kernel_regs[c.index].load(std::memory_order_relaxed);
+  const int per_cta = (r + 7) / 8 * 8 * kConsumerThreads;
+  const int k = d.regs_per_sm / per_cta;
+  return k < 8 ? k : 8;
+}
 
 // The launch of `rows` rows: the instance (*choice) and its shape.
 int shape_for(const DeviceInfo& d, int64_t rows, int64_t hidden, int n, int sm_budget,
               Choice* choice, LaunchShape* shape) {
   int grid = grid_for(d, rows, sm_budget);
-  if (sm_budget == 0 && rows > grid && rows <= 2 * static_cast<int64_t>(d.sms)) {
-    // On the whole GPU with up to two rows per SM: one direct-form CTA per
-    // row, where two such CTAs fit on an SM, instead of a ring CTA per SM
-    // that owns two rows. Interleaved at T = 160-304 against the ring: per
-    // launch never slower, from one CUDA graph 1-30% faster and back to back
-    // 1-22% faster at H = 4096 (N = 2, 4, 8) and H = 8192 (N = 2, 4); at
-    // H = 8192, N = 8 (144 registers: one CTA per SM, so two waves) 6-17%
-    // slower back to back, which the register check excludes.
+  if (sm_budget == 0 && rows > grid && rows <= 8 * static_cast<int64_t>(d.sms)) {
+    // On the whole GPU with more rows than SMs: one direct-form CTA per row
+    // while the rows fit in one wave of co-resident direct CTAs (k per SM, by
+    // registers), instead of a ring CTA per SM that owns several rows.
+    // Interleaved against the ring: at T = 160-304 (k >= 2) per launch never
+    // slower, from one CUDA graph 1-30% faster and back to back 1-22% faster
+    // at H = 4096 (N = 2, 4, 8) and H = 8192 (N = 2, 4); at T = 400-760
+    // (k = 3-5: H = 4096, N = 2, 4; H = 8192, N = 2) back to back 10-27%
+    // faster. At H = 8192, N = 8 (144 registers: k = 1, so two waves) it was
+    // 6-17% slower back to back, which the register count excludes.
     const Choice w = select_kernel(static_cast<int>(hidden / 8), n, rows, static_cast<int>(rows),
                                    d.sms);
-    if (w.direct && two_direct_ctas_fit(d, w)) grid = static_cast<int>(rows);
+    if (w.direct && rows <= static_cast<int64_t>(direct_ctas_per_sm(d, w)) * d.sms)
+      grid = static_cast<int>(rows);
   }
   const Choice c = select_kernel(static_cast<int>(hidden / 8), n, rows, grid, d.sms);
   if (c.direct) {

@@ -633,20 +633,21 @@ def test_direct_form_against_the_ring_and_the_oracle(H, N):
 
 @pytest.mark.parametrize("T,H,N", [(160, 4096, 8), (256, 4096, 2), (304, 8192, 4),
                                    (200, 6144, 2), (300, 16384, 2), (256, 8192, 8),
-                                   (305, 4096, 2)])
-def test_one_cta_per_row_up_to_two_rows_per_sm(T, H, N):
-    """On the whole GPU with more rows than SMs but at most two per SM, one
-    direct-form CTA per row where two such CTAs fit in an SM's registers, a
-    ring CTA per SM otherwise (H = 8192, N = 8: 144 registers a thread; and
-    beyond two rows per SM). Every row against the oracle, and bit for bit
-    against the same rows under an 8-SM budget (a ring form)."""
+                                   (305, 4096, 8), (608, 4096, 4), (760, 4096, 2),
+                                   (761, 4096, 2), (456, 8192, 2)])
+def test_one_cta_per_row_while_the_rows_fit_at_once(T, H, N):
+    """On the whole GPU with more rows than SMs: one direct-form CTA per row
+    while all of them fit on the GPU at once (k CTAs per SM by their
+    registers: 5 at H = 4096, N = 2; 4 at N = 4; 2 at N = 8; 1 at H = 8192,
+    N = 8), a ring CTA per SM otherwise. Every row against the oracle, and
+    bit for bit against the same rows under an 8-SM budget (a ring form)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     shape = tw.tw_launch_shape(T, H, N, 0)
     direct = shape["threads"] == 256
     assert shape["grid"] == (T if direct else min(T, sms)), shape
-    if (T, H, N) == (160, 4096, 8):
+    if (T, H, N) in ((160, 4096, 8), (608, 4096, 4), (760, 4096, 2)):
         assert direct
-    if (T, H, N) in ((256, 8192, 8), (305, 4096, 2)):
+    if (T, H, N) in ((256, 8192, 8), (305, 4096, 8), (761, 4096, 2)):
         assert not direct
     p, r, g = synth.make_inputs(T, H, N, 0.02, seed=T + H + N)
     R, out = run(p, r, g)
