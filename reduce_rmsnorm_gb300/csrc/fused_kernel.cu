@@ -947,10 +947,12 @@ int vpt_for(int n) { return n <= 8 ? 2 : 1; }
 // `grid` CTAs on a GPU of `sms` SMs. Every form gives bitwise the same rows
 // (same thread-to-vector map, same order of every sum), so the choice is by
 // speed alone. Measured back to back, interleaved, at H = 8192:
-//  * N <= 4, some CTA owning >= 4 rows: the chunk ring with two pipelines.
-//    Per SM at an 8-SM budget (T = 4096) N = 1 78 -> 102 GB/s, 2: 88 -> 116,
-//    3: 98 -> 121, 4: 107 -> 108; at full GPU 0-5% faster for T >= 1024, but
-//    6% slower with ~3 rows per CTA (T = 512, N = 4), hence the row floor.
+//  * N <= 4, some CTA owning >= 4 rows (>= 3 for N <= 2): the chunk ring
+//    with two pipelines. Per SM at an 8-SM budget (T = 4096) N = 1 78 -> 102
+//    GB/s, 2: 88 -> 116, 3: 98 -> 121, 4: 107 -> 108; at full GPU 0-5%
+//    faster for T >= 1024, but 6% slower with ~3 rows per CTA (T = 512,
+//    N = 4), hence the row floor; for N <= 2 with 3-4 rows per CTA
+//    (T = 512-600, H = 8192) 3-7% faster back to back.
 //  * N >= 9, whole-chunk rows, a grid of at most half the SMs, more rows than
 //    CTAs: the row ring with two pipelines, whose 16 KiB copies lift the
 //    per-SM rate from 83-95 to 112 GB/s at an 8-SM budget. At full GPU, where
@@ -992,7 +994,7 @@ Choice select_kernel(int vpr, int n, int64_t rows, int grid, int sms) {
   c.groups = 1;
   c.vpt = vpt;
   const int exact = vpr == (1 << k) * kSlotVec ? 1 : 0;
-  const bool four_rows = rows >= 4 * static_cast<int64_t>(grid);
+  const bool four_rows = rows >= (n <= 2 ? 3 : 4) * static_cast<int64_t>(grid);
   if (vpt == 2 && k == 2 && four_rows && (n <= 3 || (n == 4 && exact))) {
     c.groups = 2;
     c.index = 92 + exact * 4 + (n - 1);

@@ -80,8 +80,13 @@ CASES = [
     (512, 8192, 8, 6, 0, False),     # 3-4 rows per CTA: CTAs of the next step start early
     (1024, 8192, 8, 6, 0, False),    # the Llama-3.3-70B layer shape
     (333, 4104, 3, 5, 0, False),     # ragged rows and chunks, runtime N
-    (128, 4096, 2, 8, 0, False),     # the PR1 shape: one row per CTA
-    (152, 4096, 8, 6, 0, False),     # one row per CTA on every SM, a one-stage 72 KiB ring
+    (128, 4096, 2, 8, 0, False),     # the PR1 shape: one row per CTA, the direct form
+    (152, 4096, 8, 6, 0, False),     # one row per CTA on every SM, the direct form
+    (150, 16384, 8, 4, 0, False),    # one row per CTA, the direct form at KMAX = 8
+    (100, 12296, 8, 4, 0, False),    # one row per CTA, ragged KMAX = 8 at N = 8: the ring
+    (304, 4096, 8, 5, 0, False),     # one direct CTA per row, two per SM
+    (600, 3080, 2, 4, 0, False),     # one direct CTA per row, ragged, four per SM
+    (520, 8192, 2, 4, 0, False),     # two-pipeline chunk ring from 3 rows per CTA (N <= 2)
     (256, 8192, 8, 4, 8, False),     # under an SM budget of 8
     (4096, 8192, 8, 3, 0, True),     # planned 2048/2048 split on two streams, per step
     (4864, 8192, 2, 3, 16, True),    # uneven planned split under a budget

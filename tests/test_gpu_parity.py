@@ -315,20 +315,20 @@ def test_sm_budget_bitwise(budget):
 def test_kernel_forms_bitwise(H, N):
     """The launch picks among kernel forms by speed: one or two pipelines per
     CTA, chunk ring or row ring. Every form must give the same rows bit for
-    bit. T = 600 on the whole GPU (under 4 rows per CTA, a grid over half the
-    SMs) takes the one-pipeline chunk ring; an 8-SM budget takes the
+    bit. T = 300 under a 120-SM budget (2.5 rows per CTA, a grid over half
+    the SMs) takes the one-pipeline chunk ring; an 8-SM budget takes the
     two-pipeline form for these shapes. The launch shapes are checked to
     differ, so the comparison is between two forms."""
-    T = 600
-    full = tw.tw_launch_shape(T, H, N, 0)
+    T = 300
+    wide = tw.tw_launch_shape(T, H, N, 120)
     b8 = tw.tw_launch_shape(T, H, N, 8)
-    assert full["threads"] == 288 and b8["threads"] == 544, (full, b8)
+    assert wide["threads"] == 288 and b8["threads"] == 544, (wide, b8)
     p, r, g = synth.make_inputs(T, H, N, 0.02, seed=H + 3 * N)
-    ref = run(p, r, g, sm_budget=0)
+    ref = run(p, r, g, sm_budget=120)
     got = run(p, r, g, sm_budget=8)
     assert_same(ref[0], got[0])
     assert_same(ref[1], got[1])
-    rows = [0, 1, 299, 300, 598, 599] + list(range(7, 600, 37))
+    rows = [0, 1, 149, 150, 298, 299] + list(range(7, 300, 37))
     check_rows(p, r, g, EPS, got[0], got[1], rows=rows)
 
 
