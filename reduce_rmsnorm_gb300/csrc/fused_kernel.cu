@@ -12,7 +12,9 @@
 //     second CTA of this kernel fits), each owning a contiguous range of token
 //     rows ([W]'s tokens_per_cta = ceil(num_tokens / gridDim.x), balanced).
 //     The grid size is the SM budget. With one row per CTA the ring holds just
-//     that row, so a small row leaves room for the next launch's CTAs.
+//     that row, so a small row leaves room for the next launch's CTAs; the
+//     direct form (below) holds no ring at all, and on the whole GPU runs one
+//     CTA per row while all of them fit on the GPU at once.
 //   * Warp-specialised: the producer warp streams each row, in chunks of 8 KiB
 //     (N <= 8) or 4 KiB of every source (N partials + residual), from HBM into
 //     a ring of shared-memory stages with 1-D TMA bulk copies (cp.async.bulk,
