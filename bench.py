@@ -408,7 +408,9 @@ def compact_sweep(tw, dev, l2, peak, reps=20):
     """The rest of the metric in the default line: GB/s and tokens/s at
     T = 1024 / 4096 / 16384 on the whole GPU, and GB/s per SM at SM budgets
     2 / 4 / 8 / 16 for T = 8192 (H = 8192, N = 8), plus N = 2 and N = 12 at
-    an 8-SM budget (T = 4096). Inputs are made on the
+    an 8-SM budget (T = 4096), and two small batches on the whole GPU that
+    take the direct form: T = 128 (H = 8192, N = 8; one row per CTA) and
+    T = 304 (H = 4096, N = 8; one CTA per row, two per SM). Inputs are made on the
     device from a seeded generator with the workload's distributions (this
     measures time only; parity runs on the synthetic CPU inputs). Each cell
     times `reps` prepared launches back to back between one event pair, and
@@ -416,10 +418,10 @@ def compact_sweep(tw, dev, l2, peak, reps=20):
     rotate over enough sets to exceed 4x the L2, or one set is already larger
     than that."""
     import torch
-    H, eps = 8192, 1e-5
+    eps = 1e-5
     gen = torch.Generator(device=dev).manual_seed(0)
 
-    def make(T, N):
+    def make(T, N, H):
         per_set = (N + 2) * T * H * 2
         out = []
         for _ in range(max(1, math.ceil(4 * l2 / per_set))):
@@ -434,7 +436,7 @@ def compact_sweep(tw, dev, l2, peak, reps=20):
     stream = torch.cuda.Stream(dev)
     stream.wait_stream(torch.cuda.current_stream(dev))
 
-    def cell(sets, T, N, budget):
+    def cell(sets, T, N, H, budget):
         calls = [tw.FusedCall(s["P"], s["R"], s["G"], eps, s["out"], stream=stream,
                               sm_budget=budget) for s in sets]
         with torch.cuda.stream(stream):
@@ -455,27 +457,33 @@ def compact_sweep(tw, dev, l2, peak, reps=20):
         b2b = a.elapsed_time(b) * 1e3 / reps
         per = _median(x.elapsed_time(y) * 1e3 for x, y in evs)
         nbytes = tw.bytes_per_call(T, H, N)
-        used = tw.tw_launch_shape(T, H, N, budget)["grid"]
+        shape = tw.tw_launch_shape(T, H, N, budget)
+        used = min(shape["grid"], tw_sms)
+        form = {256: "direct", 288: "ring", 544: "two pipelines"}.get(shape["threads"], "?")
         gbs = nbytes / b2b / 1e3
-        return {"T": T, "N": N, "sm_budget": budget or "full", "sms_used": used,
+        return {"T": T, "H": H, "N": N, "sm_budget": budget or "full", "sms_used": used,
+                "ctas": shape["grid"], "form": form,
                 "us_b2b": round(b2b, 2), "GB_s": round(gbs, 1), "frac": round(gbs / peak, 4),
                 "GB_s_per_sm": round(gbs / used, 2), "tokens_per_s": round(T / b2b * 1e6, 1),
                 "us_per_launch": round(per, 2),
                 "GB_s_per_launch": round(nbytes / per / 1e3, 1)}
 
+    tw_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     cells = []
     # N = 8 over T and budgets; N = 2 and 12 under an 8-SM budget, where the
-    # launch takes the two-pipeline forms
-    for T, N, budgets in ((1024, 8, (0,)), (4096, 8, (0,)), (16384, 8, (0,)),
-                          (8192, 8, (2, 4, 8, 16, 0)), (4096, 2, (8,)), (4096, 12, (8,))):
-        sets = make(T, N)
+    # launch takes the two-pipeline forms; two small batches in the direct form
+    for T, N, H, budgets in ((1024, 8, 8192, (0,)), (4096, 8, 8192, (0,)),
+                             (16384, 8, 8192, (0,)), (8192, 8, 8192, (2, 4, 8, 16, 0)),
+                             (4096, 2, 8192, (8,)), (4096, 12, 8192, (8,)),
+                             (128, 8, 8192, (0,)), (304, 8, 4096, (0,))):
+        sets = make(T, N, H)
         torch.cuda.synchronize()
         for budget in budgets:
-            cells.append(cell(sets, T, N, budget))
+            cells.append(cell(sets, T, N, H, budget))
         del sets
     torch.cuda.current_stream(dev).wait_stream(stream)
     torch.cuda.empty_cache()
-    return {"H": H, "reps": reps, "cells": cells,
+    return {"reps": reps, "cells": cells,
             "timing": "us_b2b: launches back to back between one event pair (GB_s, frac, "
                       "GB_s_per_sm, tokens_per_s); us_per_launch: median of an event pair "
                       "around each launch (launch latency included)"}
@@ -966,7 +974,8 @@ def sweep(args):
             torch.cuda.synchronize()
             us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
             med = us[len(us) // 2]
-            used = tw.tw_launch_shape(T, H, N, budget)["grid"]
+            ctas = tw.tw_launch_shape(T, H, N, budget)["grid"]
+            used = min(ctas, sms)  # more CTAs than SMs: one direct CTA per row
             gbs = bytes_call / (med / 1e6) / 1e9
             # launch-overhead context: the same launches back to back (eager,
             # programmatic dependent launch) and replayed from one CUDA graph
@@ -1014,7 +1023,7 @@ def sweep(args):
                 extra.update({"unfused_us_median": round(uus, 2),
                               "fused_speedup": round(uus / med, 3)})
             print(json.dumps({"T": T, "H": H, "N": N, "sm_budget": budget or "full",
-                              "sms_used": used, "us_median": round(med, 2),
+                              "sms_used": used, "ctas": ctas, "us_median": round(med, 2),
                               "us_p10": round(us[len(us) // 10], 2),
                               "us_p90": round(us[(9 * len(us)) // 10], 2),
                               "GB_s": round(gbs, 1), "GB_s_per_sm": round(gbs / used, 2),

@@ -70,3 +70,20 @@ def test_graph_mode_captures_nothing_in_the_timed_region():
     assert d["config"]["launch"].startswith("cuda graph")
     assert d["value"] > 0
 
+
+def test_sweep_block_carries_every_form():
+    """The default line's sweep block: the one-pipeline ring on the whole GPU,
+    the two-pipeline forms under an 8-SM budget, and the direct form for the
+    two small batches (one row per CTA; one CTA per row)."""
+    lines = _run("--steps", "5", "--warmup", "3", "--no-cpu-baseline", "--e2e-steps", "3",
+                 "--no-unfused")
+    cells = {(c["T"], c["H"], c["N"], c["sm_budget"]): c for c in lines[0]["sweep"]["cells"]}
+    assert cells[(1024, 8192, 8, "full")]["form"] == "ring"
+    assert cells[(4096, 8192, 2, 8)]["form"] == "two pipelines"
+    assert cells[(4096, 8192, 12, 8)]["form"] == "two pipelines"
+    assert cells[(128, 8192, 8, "full")]["form"] == "direct"
+    d = cells[(304, 4096, 8, "full")]
+    assert d["form"] == "direct" and d["ctas"] == 304 and d["sms_used"] <= 152
+    for c in cells.values():
+        assert c["GB_s"] > 0 and c["us_b2b"] > 0
+
