@@ -978,14 +978,13 @@ Choice select_kernel(int vpr, int n, int64_t rows, int grid, int sms) {
   const int dk = log2_pow2_at_least((vpr + kSlotVec - 1) / kSlotVec);  // direct KMAX = 2^dk
   const int dexact = vpr == (1 << dk) * kSlotVec ? 1 : 0;
   if (rows <= grid && n <= 8 && dk <= 3 && kDirect[dexact][dk][n - 1] != nullptr) {
-    const int ki = dk, exact = dexact;
     c.direct = 1;
-    c.kmax = 1 << ki;
+    c.kmax = 1 << dk;
     c.rowring = 0;
     c.groups = 1;
     c.vpt = 1;  // unused
-    c.index = 102 + exact * 32 + ki * 8 + (n - 1);
-    c.fn = kDirect[exact][ki][n - 1];
+    c.index = 102 + dexact * 32 + dk * 8 + (n - 1);
+    c.fn = kDirect[dexact][dk][n - 1];
     return c;
   }
   const int vpt = vpt_for(n);
@@ -996,8 +995,8 @@ Choice select_kernel(int vpr, int n, int64_t rows, int grid, int sms) {
   c.groups = 1;
   c.vpt = vpt;
   const int exact = vpr == (1 << k) * kSlotVec ? 1 : 0;
-  const bool four_rows = rows >= (n <= 2 ? 3 : 4) * static_cast<int64_t>(grid);
-  if (vpt == 2 && k == 2 && four_rows && (n <= 3 || (n == 4 && exact))) {
+  const bool enough_rows = rows >= (n <= 2 ? 3 : 4) * static_cast<int64_t>(grid);
+  if (vpt == 2 && k == 2 && enough_rows && (n <= 3 || (n == 4 && exact))) {
     c.groups = 2;
     c.index = 92 + exact * 4 + (n - 1);
     c.fn = kChunkTwo[exact][n - 1];
